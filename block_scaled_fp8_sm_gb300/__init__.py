@@ -1,0 +1,104 @@
+"""Python binding of libbsfp8 (block-scaled E4M3 GEMM, bf16 out, sm_103a).
+
+Argument marshalling only: torch tensors are turned into device pointers and
+the current CUDA stream, and the C entry points of include/bsfp8.h are called
+by the same names.  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU or library fallback, and a non-zero status raises
+``Fp8Error``.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _abi
+from ._abi import (FP8_PATH_AUTO, FP8_PATH_NATIVE, FP8_PATH_PROMOTE,  # noqa: F401
+                   FP8_DEBUG_WAIT_LIMIT_CYCLES, FP8_DEBUG_WITHHOLD_STAGE,
+                   FP8_MAX_GROUPS_PER_LAUNCH, fp8_group_desc)
+
+__all__ = ["fp8_gemm_blockscaled", "fp8_gemm_grouped", "fp8_status_query", "fp8_strerror",
+           "fp8_version", "fp8_debug_set", "fp8_lib_shutdown", "Fp8Error", "library"]
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {fp8_strerror(code)} ({code})" if what else fp8_strerror(code))
+
+
+def library():
+    return _abi.load()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise Fp8Error(rc, what)
+
+
+def fp8_gemm_blockscaled(A, sA, B, sB, C, M=None, N=None, K=None, stream=None, mode=None):
+    """C[M,N] (bf16) = block-scaled E4M3 GEMM of A[M,K] and B[N,K] with fp32
+    32x32 block scales sA, sB.  Tensors are CUDA tensors (A/B uint8 codes or
+    float8_e4m3fn, sA/sB float32, C bfloat16).  ``mode`` None = AUTO."""
+    M = A.shape[0] if M is None else M
+    K = A.shape[1] if K is None else K
+    N = B.shape[0] if N is None else N
+    lib = library()
+    s = _stream(stream)
+    if mode is None:
+        rc = lib.fp8_gemm_blockscaled(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C), M, N, K, s)
+    else:
+        rc = lib.fp8_gemm_blockscaled_ex(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C), M, N, K,
+                                         int(mode), s)
+    _check(rc, "fp8_gemm_blockscaled")
+    return C
+
+
+def fp8_gemm_grouped(groups, Ms, N, K, G=None, stream=None, mode=None):
+    """groups: sequence of (A_g, sA_g, B_g, sB_g, C_g) CUDA tensors (or raw
+    device pointers); Ms: int32 CUDA tensor of G row counts (read on device)."""
+    G = len(groups) if G is None else G
+    arr = (fp8_group_desc * max(G, 1))()
+    for g, (a, sa, b, sb, c) in enumerate(groups[:G]):
+        arr[g] = fp8_group_desc(*[x if isinstance(x, int) else _ptr(x) for x in (a, sa, b, sb, c)])
+    lib = library()
+    s = _stream(stream)
+    ms = Ms if isinstance(Ms, int) else _ptr(Ms)
+    if mode is None:
+        rc = lib.fp8_gemm_grouped(arr, ms, N, K, G, s)
+    else:
+        rc = lib.fp8_gemm_grouped_ex(arr, ms, N, K, G, int(mode), s)
+    _check(rc, "fp8_gemm_grouped")
+
+
+def fp8_status_query(stream=None) -> int:
+    out = ctypes.c_int(0)
+    _check(library().fp8_status_query(_stream(stream), ctypes.byref(out)), "fp8_status_query")
+    return out.value
+
+
+def fp8_strerror(code: int) -> str:
+    return library().fp8_strerror(int(code)).decode()
+
+
+def fp8_version() -> int:
+    return library().fp8_version()
+
+
+def fp8_debug_set(key: int, value: int):
+    _check(library().fp8_debug_set(int(key), int(value)), "fp8_debug_set")
+
+
+def fp8_lib_shutdown():
+    library().fp8_lib_shutdown()

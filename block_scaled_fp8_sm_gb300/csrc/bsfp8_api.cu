@@ -1,0 +1,343 @@
+// bsfp8_api.cu -- host side of the C ABI declared in include/bsfp8.h:
+// argument validation, TMA descriptor encoding, per-device set-up, launches
+// and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/bsfp8.h"
+#include "gemm_kernel.cuh"
+
+namespace bsfp8 {
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int error = FP8_OK;          // sticky set-up failure (e.g. wrong architecture)
+    int sm_count = 0;
+    uint32_t *status = nullptr;  // 256-byte device allocation, word 0 used
+};
+
+std::mutex g_mu;
+DeviceState g_dev[MAX_DEVICES];
+long long g_wait_limit = -1;     // resolved lazily from the environment
+int g_withhold_stage = -1;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+constexpr long long kDefaultWaitLimit = 1ll << 31;
+
+long long wait_limit_locked() {
+    if (g_wait_limit < 0) {
+        g_wait_limit = kDefaultWaitLimit;
+        if (const char *e = std::getenv("BSFP8_WAIT_LIMIT_CYCLES")) {
+            long long v = std::atoll(e);
+            if (v > 0) g_wait_limit = v;
+        }
+    }
+    return g_wait_limit;
+}
+
+template <int BN>
+int set_kernel_attrs() {
+    if (cudaFuncSetAttribute(bsfp8_gemm_plain<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<BN>()) != cudaSuccess)
+        return FP8_ERR_CUDA;
+    if (cudaFuncSetAttribute(bsfp8_gemm_grouped<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<BN>()) != cudaSuccess)
+        return FP8_ERR_CUDA;
+    return FP8_OK;
+}
+
+// One-time set-up of the current device.  Returns FP8_OK and fills *out.
+int device_setup(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8_ERR_CUDA;
+    if (dev < 0 || dev >= MAX_DEVICES) return FP8_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (d.ready) {
+        *out = &d;
+        return d.error;
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FP8_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+        d.ready = true;
+        d.error = FP8_ERR_ARCH;
+        *out = &d;
+        return FP8_ERR_ARCH;
+    }
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return FP8_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    int rc = set_kernel_attrs<128>();
+    if (rc != FP8_OK) return rc;
+    if (!d.status) {
+        if (cudaMalloc(&d.status, 256) != cudaSuccess) return FP8_ERR_CUDA;
+        if (cudaMemset(d.status, 0, 256) != cudaSuccess) return FP8_ERR_CUDA;
+    }
+    d.sm_count = sms;
+    d.ready = true;
+    d.error = FP8_OK;
+    (void)wait_limit_locked();
+    *out = &d;
+    return FP8_OK;
+}
+
+// 2-D K-major byte tensor [rows, K] with a (BK x box_rows) box, 128-byte swizzle.
+int encode_kmajor(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_shape(int64_t M, int64_t N, int64_t K) {
+    const int64_t lim = int64_t(1) << 31;
+    if (M < 0 || N < 0 || K < 0) return FP8_ERR_SHAPE;
+    if (M >= lim || N >= lim || K >= lim) return FP8_ERR_SHAPE;
+    if ((N % 32) != 0 || (K % 32) != 0) return FP8_ERR_SHAPE;
+    return FP8_OK;
+}
+
+int check_mode(int mode) {
+    return (mode == FP8_PATH_AUTO || mode == FP8_PATH_NATIVE || mode == FP8_PATH_PROMOTE)
+               ? FP8_OK
+               : FP8_ERR_MODE;
+}
+
+int zero_fill(void *C, int64_t elems, cudaStream_t stream) {
+    const int64_t n16 = (elems * 2) / 16;
+    const int64_t tail = (elems * 2) % 16;
+    if (n16 > 0) {
+        int blocks = static_cast<int>(n16 / 256 + 1);
+        if (blocks > 4096) blocks = 4096;
+        bsfp8_zero_fill<<<blocks, 256, 0, stream>>>(static_cast<uint4 *>(C), n16);
+        if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
+    }
+    if (tail) {   // N % 32 == 0 makes rows 64-byte multiples: no tail can occur
+        return FP8_ERR_SHAPE;
+    }
+    return FP8_OK;
+}
+
+void fill_common(Common &c, int64_t M, int64_t N, int64_t K, int mode, DeviceState *d, int BN) {
+    std::memset(&c, 0, sizeof c);
+    c.M = static_cast<int>(M);
+    c.N = static_cast<int>(N);
+    c.K = static_cast<int>(K);
+    c.KB = static_cast<int>(K / 32);
+    c.KS = static_cast<int>((K + BK - 1) / BK);
+    c.mt = static_cast<int>((M + BM - 1) / BM);
+    c.nt = static_cast<int>((N + BN - 1) / BN);
+    c.num_tiles = c.mt * c.nt;
+    c.mode = mode;
+    c.status = d->status;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        c.wait_limit = wait_limit_locked();
+        c.withhold_stage = g_withhold_stage;
+    }
+}
+
+template <int BN>
+int launch_plain(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                 int64_t M, int64_t N, int64_t K, int mode, DeviceState *d, cudaStream_t stream) {
+    PlainArgs args;
+    std::memset(&args, 0, sizeof args);
+    fill_common(args.c, M, N, K, mode, d, BN);
+    int rc = encode_kmajor(&args.tmA, A, M, K, BM);
+    if (rc != FP8_OK) return rc;
+    rc = encode_kmajor(&args.tmB, B, N, K, BN);
+    if (rc != FP8_OK) return rc;
+    args.e.A = static_cast<const uint8_t *>(A);
+    args.e.sA = sA;
+    args.e.sB = sB;
+    args.e.C = static_cast<__nv_bfloat16 *>(C);
+    int grid = args.c.num_tiles < d->sm_count ? args.c.num_tiles : d->sm_count;
+    bsfp8_gemm_plain<BN><<<grid, NUM_THREADS, smem_bytes<BN>(), stream>>>(args);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+template <int BN>
+int launch_grouped(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, int64_t K,
+                   int32_t G, int mode, DeviceState *d, cudaStream_t stream) {
+    static_assert(sizeof(GroupedArgs) < 32000, "kernel parameter space");
+    GroupedArgs *args = new GroupedArgs;   // large: keep it off the stack
+    std::memset(args, 0, sizeof *args);
+    fill_common(args->c, 0, N, K, mode, d, BN);
+    args->c.G = G;
+    args->c.Ms = Ms;
+    for (int g = 0; g < G; ++g) {
+        // rows are only bounded by the tensor map; the kernel never requests
+        // B rows beyond N, so the map's row count is exactly N.
+        int rc = encode_kmajor(&args->tmB[g], groups[g].B, N, K, BN);
+        if (rc != FP8_OK) {
+            delete args;
+            return rc;
+        }
+        args->e[g].A = static_cast<const uint8_t *>(groups[g].A);
+        args->e[g].sA = groups[g].sA;
+        args->e[g].sB = groups[g].sB;
+        args->e[g].C = static_cast<__nv_bfloat16 *>(groups[g].C);
+    }
+    bsfp8_gemm_grouped<BN><<<d->sm_count, NUM_THREADS, smem_bytes<BN>(), stream>>>(*args);
+    delete args;
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace bsfp8
+
+using namespace bsfp8;
+
+extern "C" {
+
+int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const float *sB,
+                            void *C, int64_t M, int64_t N, int64_t K, int mode,
+                            cudaStream_t stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != FP8_OK) return rc;
+    rc = check_mode(mode);
+    if (rc != FP8_OK) return rc;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!C) return FP8_ERR_NULL;
+    if (!aligned(C, 16)) return FP8_ERR_ALIGN;
+    if (K > 0) {
+        if (!A || !B || !sA || !sB) return FP8_ERR_NULL;
+        if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 4) || !aligned(sB, 4))
+            return FP8_ERR_ALIGN;
+    }
+    DeviceState *d = nullptr;
+    rc = device_setup(&d);
+    if (rc != FP8_OK) return rc;
+    if (K == 0) return zero_fill(C, M * N, stream);
+    return launch_plain<128>(A, sA, B, sB, C, M, N, K, mode, d, stream);
+}
+
+int fp8_gemm_blockscaled(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                         int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    return fp8_gemm_blockscaled_ex(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, stream);
+}
+
+int fp8_gemm_grouped_ex(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, int64_t K,
+                        int32_t G, int mode, cudaStream_t stream) {
+    int rc = check_shape(0, N, K);
+    if (rc != FP8_OK) return rc;
+    rc = check_mode(mode);
+    if (rc != FP8_OK) return rc;
+    if (G < 0) return FP8_ERR_SHAPE;
+    if (G == 0 || N == 0) return FP8_OK;
+    if (!groups || !Ms) return FP8_ERR_NULL;
+    if (!aligned(Ms, 4)) return FP8_ERR_ALIGN;
+    for (int g = 0; g < G; ++g) {
+        const fp8_group_desc &e = groups[g];
+        if (!e.A || !e.B || !e.sA || !e.sB || !e.C) return FP8_ERR_NULL;
+        if (!aligned(e.A, 16) || !aligned(e.B, 16) || !aligned(e.C, 16) || !aligned(e.sA, 4) ||
+            !aligned(e.sB, 4))
+            return FP8_ERR_ALIGN;
+    }
+    DeviceState *d = nullptr;
+    rc = device_setup(&d);
+    if (rc != FP8_OK) return rc;
+    if (K == 0) return FP8_ERR_SHAPE;   // row counts are on the device: no host-side zero fill
+    for (int32_t g0 = 0; g0 < G; g0 += FP8_MAX_GROUPS_PER_LAUNCH) {
+        const int32_t n = (G - g0) < FP8_MAX_GROUPS_PER_LAUNCH ? (G - g0) : FP8_MAX_GROUPS_PER_LAUNCH;
+        rc = launch_grouped<128>(groups + g0, Ms + g0, N, K, n, mode, d, stream);
+        if (rc != FP8_OK) return rc;
+    }
+    return FP8_OK;
+}
+
+int fp8_gemm_grouped(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, int64_t K,
+                     int32_t G, cudaStream_t stream) {
+    return fp8_gemm_grouped_ex(groups, Ms, N, K, G, FP8_PATH_AUTO, stream);
+}
+
+int fp8_status_query(cudaStream_t stream, int *status) {
+    if (!status) return FP8_ERR_NULL;
+    DeviceState *d = nullptr;
+    int rc = device_setup(&d);
+    if (rc != FP8_OK) return rc;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, d->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FP8_ERR_CUDA;
+    if (word != 0 && cudaMemset(d->status, 0, sizeof word) != cudaSuccess) return FP8_ERR_CUDA;
+    *status = (word & STATUS_TIMEOUT) ? FP8_ERR_TIMEOUT : (word & STATUS_SCALE) ? FP8_ERR_SCALE : FP8_OK;
+    return FP8_OK;
+}
+
+const char *fp8_strerror(int code) {
+    switch (code) {
+        case FP8_OK: return "FP8_OK";
+        case FP8_ERR_NULL: return "FP8_ERR_NULL: a required pointer is NULL";
+        case FP8_ERR_SHAPE: return "FP8_ERR_SHAPE: bad size (negative, N or K not a multiple of 32, >= 2^31, or G)";
+        case FP8_ERR_ALIGN: return "FP8_ERR_ALIGN: A/B/C must be 16-byte and sA/sB 4-byte aligned";
+        case FP8_ERR_ARCH: return "FP8_ERR_ARCH: the current device is not sm_103";
+        case FP8_ERR_CUDA: return "FP8_ERR_CUDA: a CUDA call failed";
+        case FP8_ERR_MODE: return "FP8_ERR_MODE: unknown path mode or debug key";
+        case FP8_ERR_SCALE: return "FP8_ERR_SCALE: native path forced with a scale that is not a power of two";
+        case FP8_ERR_TIMEOUT: return "FP8_ERR_TIMEOUT: a device-side wait ran out";
+        default: return "unknown FP8 status code";
+    }
+}
+
+int fp8_version(void) { return BSFP8_VERSION; }
+
+int fp8_debug_set(int key, int64_t value) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    switch (key) {
+        case FP8_DEBUG_WAIT_LIMIT_CYCLES:
+            g_wait_limit = value > 0 ? value : kDefaultWaitLimit;
+            return FP8_OK;
+        case FP8_DEBUG_WITHHOLD_STAGE:
+            g_withhold_stage = value >= 0 ? static_cast<int>(value) : -1;
+            return FP8_OK;
+        default:
+            return FP8_ERR_MODE;
+    }
+}
+
+void fp8_lib_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < MAX_DEVICES; ++i) {
+        if (g_dev[i].status) {
+            int cur = 0;
+            if (cudaGetDevice(&cur) == cudaSuccess && cudaSetDevice(i) == cudaSuccess) {
+                cudaFree(g_dev[i].status);
+                cudaSetDevice(cur);
+            }
+        }
+        g_dev[i] = DeviceState();
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+/*
+ * bsfp8.h -- C ABI of libbsfp8: block-scaled E4M3 GEMM with bf16 output on one
+ * GB300 (sm_103a).
+ *
+ * Operation (FP8 GEMM library article, hncyxsy.com/news/241433, section 2.2
+ * "scale granularity" and section 2.3 "where the scales live": one fp32 scale
+ * per 32x32 block of each operand, taking part in the accumulation, no separate
+ * dequantisation pass; section 6 gives the operand shapes A [M,K], B [N,K],
+ * scale_a [M/32,K/32], scale_b [N/32,K/32]):
+ *
+ *   C[m,n] = bf16( sum_kb sA[m/32][kb] * sB[n/32][kb] * sum_{k in kb} A[m,k]*B[n,k] )
+ *
+ * kb runs over the K/32 blocks of 32 consecutive k in ascending order.  The
+ * K-reduction order is the same for every M: no split-K, no shape-dependent
+ * tile configuration ("AI Infra 进阶：如何让大模型输出确定的结果",
+ * aif.amtbbs.org post 29992, section 1: a row's result changes with the batch
+ * only through the reduction split).  Hence every output row is bit-identical
+ * whatever M (and whatever other rows) it is computed with, given the same
+ * path (see FP8_PATH_*).
+ *
+ * Layouts (all device memory, all row-major, caller-owned):
+ *   A   [M, K]           E4M3 codes, one byte each (row stride K bytes)
+ *   B   [N, K]           E4M3 codes, K contiguous ("K-major" weights)
+ *   sA  [ceil(M/32), K/32] fp32 (the last row block may be partial)
+ *   sB  [N/32, K/32]     fp32
+ *   C   [M, N]           bf16, fully overwritten (no beta*C term)
+ *
+ * Constraints: M >= 0; N and K multiples of 32 (N, K >= 0); M, N, K < 2^31.
+ * A, B and C 16-byte aligned; sA and sB 4-byte aligned.  E4M3 NaN codes
+ * (0x7F, 0xFF) and NaN/inf scales give undefined values (never a fault).
+ *
+ * Execution: every call is asynchronous on `stream` (0 = legacy default
+ * stream), allocates no per-call device memory and never synchronises the
+ * host.  The first call on a device does a one-time set-up for that device
+ * (kernel attributes, a 256-byte device status word); make it outside any
+ * stream capture.  Calls are thread-safe.
+ *
+ * Errors: functions return FP8_OK (0) or a negative FP8_ERR_* code; argument
+ * errors are detected on the host before anything is enqueued.  Conditions
+ * found on the device (a bounded wait that ran out, a forced native path with
+ * non-power-of-two scales) are recorded in a sticky per-device status word
+ * read by fp8_status_query().
+ */
+#ifndef BSFP8_H
+#define BSFP8_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BSFP8_VERSION 10000 /* 1.0.0 */
+
+enum {
+    FP8_OK = 0,
+    FP8_ERR_NULL = -1,       /* a required pointer is NULL */
+    FP8_ERR_SHAPE = -2,      /* negative size, N or K not a multiple of 32, size >= 2^31, G out of range */
+    FP8_ERR_ALIGN = -3,      /* A/B/C not 16-byte aligned or sA/sB not 4-byte aligned */
+    FP8_ERR_ARCH = -4,       /* current device is not sm_103 */
+    FP8_ERR_CUDA = -5,       /* a CUDA runtime/driver call failed (launch, attribute, ...) */
+    FP8_ERR_MODE = -6,       /* unknown path mode or debug key */
+    FP8_ERR_SCALE = -7,      /* device status: FP8_PATH_NATIVE with a scale that is not 2^e */
+    FP8_ERR_TIMEOUT = -8     /* device status: a bounded wait inside a kernel ran out */
+};
+
+/* Path selection.
+ * FP8_PATH_AUTO: per output tile (128 rows x BN columns), the native path is
+ *   taken when every scale the tile reads (its row blocks of sA and column
+ *   blocks of sB, all of K) is a positive normal power of two; otherwise the
+ *   promotion path.  A row's bits therefore depend only on the scales of the
+ *   rows in its own 128-row tile (rows 128*floor(m/128) ...).
+ * FP8_PATH_NATIVE: block-scaled tensor-core path (kind::mxf8f6f4 with UE8M0
+ *   scales, exact for power-of-two scales).  A tile that finds another scale
+ *   is computed by the promotion path and FP8_ERR_SCALE is recorded.
+ * FP8_PATH_PROMOTE: per-K-block fp32 promotion for arbitrary fp32 scales:
+ *   unscaled 32-deep tensor-core partials, scaled and accumulated in fp32. */
+enum { FP8_PATH_AUTO = 0, FP8_PATH_NATIVE = 1, FP8_PATH_PROMOTE = 2 };
+
+/* Block-scaled GEMM, AUTO path.  Returns FP8_OK or FP8_ERR_*.
+ * M == 0, N == 0: nothing is enqueued.  K == 0: C is zero-filled. */
+int fp8_gemm_blockscaled(const void *A, const float *sA, const void *B, const float *sB,
+                         void *C, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/* Same with an explicit path (FP8_PATH_*). */
+int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const float *sB,
+                            void *C, int64_t M, int64_t N, int64_t K, int mode,
+                            cudaStream_t stream);
+
+/* One group of a grouped launch: device pointers with the layouts above,
+ * sized by that group's M_g (sA_g has ceil(M_g/32) group-local row blocks). */
+typedef struct fp8_group_desc {
+    const void *A;    /* [M_g, K] E4M3 */
+    const float *sA;  /* [ceil(M_g/32), K/32] fp32 */
+    const void *B;    /* [N, K] E4M3 */
+    const float *sB;  /* [N/32, K/32] fp32 */
+    void *C;          /* [M_g, N] bf16 */
+} fp8_group_desc;
+
+#define FP8_MAX_GROUPS_PER_LAUNCH 64
+
+/* Grouped GEMM for ragged decode batches (FP8 GEMM library article, section
+ * 4.1-4.2: many small GEMMs of different shapes merged into one launch, each
+ * block finding its problem from a parameter table; section 4.3: shapes kept
+ * in device memory so a captured CUDA graph stays valid when they change).
+ *
+ * groups: HOST array of G descriptors (copied into the launch; the caller may
+ *         reuse it as soon as the call returns).
+ * Ms:     DEVICE int32[G], the row count of each group, read only by the
+ *         kernel (so it may change between graph replays).  M_g < 0 is
+ *         treated as 0.
+ * N, K:   shared by all groups (multiples of 32).
+ * Groups are independent GEMMs: group g's result is bit-identical to
+ * fp8_gemm_blockscaled on that group alone with the same path.
+ * G <= FP8_MAX_GROUPS_PER_LAUNCH runs as one launch; larger G is split into
+ * consecutive launches of at most that many groups on the same stream. */
+int fp8_gemm_grouped(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, int64_t K,
+                     int32_t G, cudaStream_t stream);
+
+int fp8_gemm_grouped_ex(const fp8_group_desc *groups, const int32_t *Ms, int64_t N,
+                        int64_t K, int32_t G, int mode, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word.  *status = FP8_OK, or the FP8_ERR_* code of the condition recorded
+ * first since the last query (FP8_ERR_TIMEOUT takes precedence).  Returns
+ * FP8_OK or FP8_ERR_CUDA / FP8_ERR_NULL. */
+int fp8_status_query(cudaStream_t stream, int *status);
+
+/* Human-readable name of an FP8_* code (static storage). */
+const char *fp8_strerror(int code);
+
+/* BSFP8_VERSION of the loaded library. */
+int fp8_version(void);
+
+/* Debug/test controls (process-wide, affect launches enqueued afterwards).
+ * FP8_DEBUG_WAIT_LIMIT_CYCLES: SM clock cycles a device-side wait may spin
+ *   before the kernel records FP8_ERR_TIMEOUT and returns cleanly (default
+ *   2^31, about one second; the environment variable BSFP8_WAIT_LIMIT_CYCLES
+ *   sets the initial value).  value <= 0 restores the default.
+ * FP8_DEBUG_WITHHOLD_STAGE: when >= 0, the producer of CTA 0 never loads
+ *   that pipeline stage (counted from 0 over the CTA's whole K loop), so the
+ *   waits behind it run out; the output is then incomplete.  -1 (default)
+ *   disables it.  Used by the bounded-wait test.
+ * Returns FP8_OK or FP8_ERR_MODE for an unknown key. */
+enum { FP8_DEBUG_WAIT_LIMIT_CYCLES = 1, FP8_DEBUG_WITHHOLD_STAGE = 2 };
+int fp8_debug_set(int key, int64_t value);
+
+/* Frees the per-device status words.  Later calls set them up again. */
+void fp8_lib_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BSFP8_H */
