@@ -1,0 +1,451 @@
+"""Benchmark of the block-scaled E4M3 GEMM library on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one block-scaled GEMM of the headline workload (M=N=K=4096,
+power-of-two 32x32 scales, bf16 out) with inputs resident in HBM; the L2 is
+flushed (a 512 MiB write) between timed steps and each step is timed with CUDA
+events on the launching stream.  The same JSON line also carries the other
+workloads measured the same way: the 8192x28672x8192 prefill projection, the
+grouped decode batch (G=16, M_g in [1,64], N=4096, K=7168; GB/s against HBM)
+and the 8192^3 arbitrary-scale GEMM with outliers (promotion path).
+
+``--impl reference`` times the CPU oracle (the only other implementation of
+the method; plain C, fp64) on a bounded sample of the same workload.
+
+Multi-GPU: the GEMM runs as independent replicas, one per rank (weak scaling);
+ranks only meet for the timing barrier and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MEASURED = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+L2_FLUSH_BYTES = 512 << 20
+
+HEADLINE = "c1"
+WORKLOAD_NAMES = {
+    "c1": "block-scaled E4M3 GEMM M=N=K=4096, pow2 32x32 scales, bf16 out",
+    "c2": "prefill projection GEMM M=8192 N=28672 K=8192, pow2 32x32 scales",
+    "c3": "grouped decode G=16 M_g~U[1,64] N=4096 K=7168, per-group B, pow2 scales",
+    "c4": "arbitrary-scale GEMM M=N=K=8192 (amax/448 scales, 0.5% x50 outliers)",
+}
+
+
+def peaks():
+    src = "measured"
+    try:
+        with open(MEASURED) as f:
+            p = json.load(f)
+    except Exception:
+        p, src = dict(FALLBACK), "fallback"
+    return p, src
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_scaled_fp8_sm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the kernel source as it is now."""
+    try:
+        with open(TRAFFIC) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    e = t.get(workload)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- ours ----
+
+def make_runner(name, dev, bs):
+    """Returns (run(stream), flops, algorithmic bytes) for one workload with
+    its inputs on the device."""
+    import torch
+
+    import workloads
+    p = workloads.make(name, seed=0, device=dev)
+    if name == "c3":
+        Cs = [torch.empty(m, p.N, dtype=torch.bfloat16, device=dev) for m in p.Ms]
+        groups = [(p.A[o:o + m], sa, b, sb, c) for o, m, sa, b, sb, c in
+                  zip(p.offsets, p.Ms, p.sA, p.B, p.sB, Cs)]
+        Ms = torch.tensor(p.Ms, dtype=torch.int32, device=dev)
+
+        def run(stream):
+            bs.fp8_gemm_grouped(groups, Ms, p.N, p.K, stream=stream)
+        return run, p.flops, p.algorithmic_bytes
+    C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
+
+    def run(stream):
+        bs.fp8_gemm_blockscaled(p.A, p.sA, p.B, p.sB, C, p.M, p.N, p.K, stream=stream)
+    return run, p.flops, p.algorithmic_bytes
+
+
+def time_device(run, steps, warmup, dev, flush_buf, world):
+    """Per-step kernel time (ms) with CUDA events on the launching stream."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        run(stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        flush_buf.fill_(i & 0xFF)          # evict the operands from L2
+        ev[i][0].record(stream)
+        run(stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def time_e2e(name, steps, warmup, dev, bs, world):
+    """Same metric through the public API with pinned HOST buffers: each step
+    copies the inputs host->device, runs the GEMM and reads C back."""
+    import torch
+
+    import workloads
+    p = workloads.make(name, seed=0, device="cpu")
+    hA, hsA, hB, hsB = (t.pin_memory() for t in (p.A, p.sA, p.B, p.sB))
+    hC = torch.empty(p.M, p.N, dtype=torch.bfloat16).pin_memory()
+    dA, dsA, dB, dsB = (torch.empty_like(t, device=dev) for t in (hA, hsA, hB, hsB))
+    dC = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for d, h in ((dA, hA), (dsA, hsA), (dB, hB), (dsB, hsB)):
+            d.copy_(h, non_blocking=True)
+        bs.fp8_gemm_blockscaled(dA, dsA, dB, dsB, dC, p.M, p.N, p.K, stream=stream)
+        hC.copy_(dC, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = t0.elapsed_time(t1) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (hA, hsA, hB, hsB))
+    d2h = hC.numel() * hC.element_size()
+    return ms, p.flops, h2d, d2h
+
+
+def cpu_baseline_sample(name, seconds=15.0):
+    """The oracle, as it is, on a bounded sample of the workload's outputs."""
+    import numpy as np
+
+    import oracle
+    import workloads
+    p = workloads.make(name, seed=0, device="cpu")
+    A, sA, B, sB = (t.numpy() for t in (p.A, p.sA, p.B, p.sB))
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    n = 256
+    spent, done = 0.0, 0
+    t_start = time.perf_counter()
+    while spent < seconds:
+        ms = rng.integers(0, p.M, n)
+        ns = rng.integers(0, p.N, n)
+        t0 = time.perf_counter()
+        oracle.gemm_sampled(A, sA, B, sB, p.M, p.N, p.K, ms, ns, nthreads=cores)
+        spent += time.perf_counter() - t0
+        done += n
+        if spent < 0.5 * seconds:
+            n *= 2
+        if time.perf_counter() - t_start > 3 * seconds:
+            break
+    tflops = 2.0 * p.K * done / spent / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} random output elements of {name} ({p.M}x{p.N}x{p.K}), "
+                      f"{spent:.1f} s, fp64 oracle on all host threads"}
+
+
+def run_ours(args):
+    import torch
+
+    import block_scaled_fp8_sm_gb300 as bs
+    from block_scaled_fp8_sm_gb300 import build
+    world, rank, local = dist_init()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        build.build()
+    barrier(world)
+    bs.library()
+    pk, pk_src = peaks()
+    fp8_peak = pk["bf16_tflops"] * FP8_PER_BF16
+    hbm_peak = pk["hbm_gbs"]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    results = {}
+    names = [HEADLINE] + ([] if args.headline_only else ["c2", "c3", "c4"])
+    if args.only:
+        names = [args.only]
+    with ClockSampler(local) as clk:
+        for name in names:
+            run, flops, nbytes = make_runner(name, dev, bs)
+            ms = time_device(run, args.steps, args.warmup, dev, flush, world)
+            mean_ms = max_over_ranks(sum(ms) / len(ms), world)
+            results[name] = {"ms": mean_ms, "flops": flops, "bytes": nbytes,
+                             "ms_min": min(ms), "ms_median": statistics.median(ms)}
+            del run
+            torch.cuda.empty_cache()
+    status = bs.fp8_status_query()
+    if status != 0:
+        raise RuntimeError(f"device status after the bench: {bs.fp8_strerror(status)}")
+    if args.only:
+        r = results[args.only]
+        if rank == 0:
+            print(json.dumps({"only": args.only, "ms_per_step": r["ms"], "ms_min": r["ms_min"],
+                              "tflops": r["flops"] / (r["ms"] * 1e-3) / 1e12,
+                              "gbs": r["bytes"] / (r["ms"] * 1e-3) / 1e9}))
+        return
+    e2e = time_e2e(HEADLINE, max(3, args.steps // 5), args.warmup, dev, bs, world)
+
+    if rank != 0:
+        return
+    h = results[HEADLINE]
+    tflops = world * h["flops"] / (h["ms"] * 1e-3) / 1e12
+
+    def roofline(name):
+        r = results[name]
+        if name == "c3":
+            ach = r["bytes"] / (r["ms"] * 1e-3) / 1e9
+            return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(ach / hbm_peak, 4), "traffic": recorded_traffic(name),
+                    "peak_source": f"{pk_src} HBM copy bandwidth"}
+        ach = r["flops"] / (r["ms"] * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4),
+                "traffic": recorded_traffic(name),
+                "peak_source": f"{pk_src} bf16 burst x {FP8_PER_BF16} (nominal fp8/bf16 ratio)"}
+
+    extra = {}
+    for name in names[1:]:
+        r = results[name]
+        entry = {"workload": WORKLOAD_NAMES[name], "ms_per_step": round(r["ms"], 4),
+                 "roofline": roofline(name)}
+        if name == "c3":
+            entry["value"] = round(r["bytes"] / (r["ms"] * 1e-3) / 1e9, 1)
+            entry["unit"] = "GB/s"
+            entry["algorithmic_bytes"] = r["bytes"]
+        else:
+            entry["value"] = round(r["flops"] / (r["ms"] * 1e-3) / 1e12, 1)
+            entry["unit"] = "TFLOP/s"
+        extra[name] = entry
+
+    line = {
+        "metric": "block-scaled FP8 GEMM TFLOPS (% FP8 peak); grouped decode GB/s (% HBM)",
+        "value": round(tflops, 1),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(h["ms"], 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 accumulate -> bf16",
+        "data": "synthetic (seeded; shapes and value distributions of the workloads)",
+        "config": {"workload": WORKLOAD_NAMES[HEADLINE], "M": 4096, "N": 4096, "K": 4096,
+                   "l2": "flushed between timed steps (512 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline(HEADLINE),
+        "gpu_launches": args.steps * len(names),
+        "clocks": clk.summary(),
+        "extra": extra,
+    }
+    if e2e:
+        ms_e2e, fl, h2d, d2h = e2e
+        line["e2e"] = {"value": round(world * fl / (ms_e2e * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(ms_e2e, 4)}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(HEADLINE, seconds=args.cpu_seconds)
+    print(json.dumps(line))
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm, on rank 0 only."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import workloads
+    p = workloads.make(HEADLINE, seed=0, device="cpu")
+    A, sA, B, sB = (t.numpy() for t in (p.A, p.sA, p.B, p.sB))
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(1)
+    n = args.ref_elements
+
+    def step():
+        ms = rng.integers(0, p.M, n)
+        ns = rng.integers(0, p.N, n)
+        oracle.gemm_sampled(A, sA, B, sB, p.M, p.N, p.K, ms, ns, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    tflops = 2.0 * p.K * n / dt / 1e12
+    sample = f"{n} random output elements of {HEADLINE} per step ({p.M}x{p.N}x{p.K})"
+    line = {
+        "impl": "reference",
+        "metric": "block-scaled FP8 GEMM TFLOPS (% FP8 peak); grouped decode GB/s (% HBM)",
+        "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD_NAMES[HEADLINE], "M": 4096, "N": 4096, "K": 4096},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-elements", type=int, default=65536)
+    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4"], default=None,
+                    help="time one workload only (no e2e, no CPU baseline): profiling runs")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -9,7 +9,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/bsfp8.h"
+#include "bsfp8.h"
 #include "gemm_kernel.cuh"
 
 namespace bsfp8 {
