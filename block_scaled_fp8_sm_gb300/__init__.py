@@ -12,7 +12,7 @@ import ctypes
 
 from . import _abi
 from ._abi import (FP8_PATH_AUTO, FP8_PATH_NATIVE, FP8_PATH_PROMOTE,  # noqa: F401
-                   FP8_DEBUG_WAIT_LIMIT_CYCLES, FP8_DEBUG_WITHHOLD_STAGE,
+                   FP8_DEBUG_WAIT_LIMIT_CYCLES, FP8_DEBUG_WITHHOLD_STAGE, FP8_DEBUG_TRACE_BUFFER,
                    FP8_MAX_GROUPS_PER_LAUNCH, fp8_group_desc)
 
 __all__ = ["fp8_gemm_blockscaled", "fp8_gemm_grouped", "fp8_status_query", "fp8_strerror",

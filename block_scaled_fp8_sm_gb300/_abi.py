@@ -27,6 +27,7 @@ FP8_PATH_PROMOTE = 2
 
 FP8_DEBUG_WAIT_LIMIT_CYCLES = 1
 FP8_DEBUG_WITHHOLD_STAGE = 2
+FP8_DEBUG_TRACE_BUFFER = 3
 
 FP8_MAX_GROUPS_PER_LAUNCH = 64
 

@@ -28,6 +28,7 @@ std::mutex g_mu;
 DeviceState g_dev[MAX_DEVICES];
 long long g_wait_limit = -1;     // resolved lazily from the environment
 int g_withhold_stage = -1;
+unsigned long long *g_trace = nullptr;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -164,6 +165,7 @@ void fill_common(Common &c, int64_t M, int64_t N, int64_t K, int mode, DeviceSta
         std::lock_guard<std::mutex> lk(g_mu);
         c.wait_limit = wait_limit_locked();
         c.withhold_stage = g_withhold_stage;
+        c.trace = g_trace;
     }
 }
 
@@ -320,6 +322,9 @@ int fp8_debug_set(int key, int64_t value) {
             return FP8_OK;
         case FP8_DEBUG_WITHHOLD_STAGE:
             g_withhold_stage = value >= 0 ? static_cast<int>(value) : -1;
+            return FP8_OK;
+        case FP8_DEBUG_TRACE_BUFFER:
+            g_trace = reinterpret_cast<unsigned long long *>(static_cast<uintptr_t>(value));
             return FP8_OK;
         default:
             return FP8_ERR_MODE;

@@ -67,6 +67,8 @@ struct Cfg {
     static constexpr int TMEM_USED = ACC_COLS + STAGES * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
     static constexpr int EPI_COLS = BN / 2;                         // columns per epilogue warp
+    static constexpr int SC_FLOATS = 64;                            // staged fp32 scales per stage: 16 A + up to 32 B
+    static constexpr int PS_FLOATS = 4 * (BN / 32);                 // scale products per K block (promotion)
     static_assert(TMEM_USED <= 512, "tensor memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
 };
@@ -87,7 +89,30 @@ struct Common {
     uint32_t *status;
     long long wait_limit;
     int withhold_stage;
+    unsigned long long *trace;   // optional event trace of CTA 0 (see trace_event)
 };
+
+// Event trace (profiling aid, off when the pointer is null): CTA 0 records the
+// SM clock of pipeline events into trace[event * TRACE_SLOTS + index].
+constexpr int TRACE_SLOTS = 1024;
+enum : int {
+    TR_PROD_EMPTY_OK = 0,   // producer: slot free, about to issue stage `it`
+    TR_MMA_FULL_OK = 1,     // MMA warp: stage `it` landed
+    TR_MMA_ISSUED = 2,      // MMA warp: stage `it` MMAs issued and committed
+    TR_EPI_FULL_OK = 3,     // epilogue warp 4: accumulator / partial `u` ready
+    TR_EPI_RELEASED = 4,    // epilogue warp 4: accumulator / partial `u` released
+    TR_MMA_BUF_OK = 5,      // MMA warp: buffer `u` free
+    TR_VERDICT = 6,         // verdict warp: tile `i` published
+    TR_MMA_LINES = 7,       // MMA warp: scale lines of stage `it` written and fenced
+    TR_MMA_CP = 8,          // MMA warp: scale copies of stage `it` issued
+    TR_MMA_MMA = 9,         // MMA warp: MMAs of stage `it` issued (before the commit)
+    TR_EVENTS = 10
+};
+
+__device__ __forceinline__ void trace_event(const Common &c, int ev, int idx) {
+    if (c.trace != nullptr && blockIdx.x == 0 && idx >= 0 && idx < TRACE_SLOTS)
+        c.trace[ev * TRACE_SLOTS + idx] = static_cast<unsigned long long>(clock64());
+}
 
 struct PlainArgs {
     CUtensorMap tmA;
@@ -108,6 +133,7 @@ struct Ctrl {
     uint64_t empty[STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t pfull[2];
     uint64_t vfull[2];
     uint64_t vempty[2];
     uint64_t drain;
@@ -126,8 +152,8 @@ struct Tile {
 template <int BN>
 constexpr int smem_bytes() {
     using C = Cfg<BN>;
-    return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES + C::SF_BYTES) +
-           static_cast<int>(sizeof(Ctrl<C::STAGES>));
+    return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES + C::SF_BYTES + 4 * C::SC_FLOATS) +
+           2 * 4 * C::PS_FLOATS + static_cast<int>(sizeof(Ctrl<C::STAGES>));
 }
 
 // ---------------------------------------------------------------------------
@@ -205,29 +231,33 @@ struct Sched {
     }
 };
 
-// Scales of one pipeline stage as this lane holds them: lane l < 16 carries
-// sA[row block l/4][kb l%4], lane l < 4*BN/32 carries sB[row block l/4][kb l%4].
-// Absent blocks read as 1.0 (UE8M0 127): they only meet zero-filled or
-// discarded rows.
-template <int BN, bool GROUPED, typename S>
-__device__ __forceinline__ void load_stage_scales(const S &sch, int j, int total, int lane,
-                                                  float &va, float &vb) {
-    va = 1.0f;
-    vb = 1.0f;
-    if (j >= total) return;
-    const Common &c = sch.c;
-    const Tile tt = sch.tile(blockIdx.x + (j / c.KS) * gridDim.x);
-    const GroupEntry &e = sch.entry(tt.g);
-    const int kb = (j % c.KS) * KB_PER_STAGE + (lane & 3);
-    if (kb >= c.KB) return;
-    const int MB = (tt.Mg + 31) / 32;
-    if (lane < 16) {
-        const int mb = tt.m0 / 32 + (lane >> 2);
-        if (mb < MB) va = __ldg(e.sA + static_cast<int64_t>(mb) * c.KB + kb);
+// 32 consecutive bf16 outputs (64 bytes, 16-byte aligned) from fp32 bits / values.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t (&r)[32]) {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t o[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(r[8 * w + 2 * x]),
+                                                      __uint_as_float(r[8 * w + 2 * x + 1]));
+            o[x] = *reinterpret_cast<uint32_t *>(&pr);
+        }
+        d[w] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    if (lane < 4 * (BN / 32)) {
-        const int nb = tt.n0 / 32 + (lane >> 2);
-        if (nb < c.N / 32) vb = __ldg(e.sB + static_cast<int64_t>(nb) * c.KB + kb);
+}
+
+__device__ __forceinline__ void store_bf16x32f(__nv_bfloat16 *dst, const float *v) {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t o[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            __nv_bfloat162 pr = __floats2bfloat162_rn(v[8 * w + 2 * x], v[8 * w + 2 * x + 1]);
+            o[x] = *reinterpret_cast<uint32_t *>(&pr);
+        }
+        d[w] = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -238,6 +268,7 @@ template <int BN, bool GROUPED, typename Args>
 __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     using C = Cfg<BN>;
     constexpr int S = C::STAGES;
+    constexpr int NBB = BN / 32;          // column blocks of B per tile
     constexpr uint32_t FULL = 0xFFFFFFFFu;
     const Common &c = args.c;
 
@@ -246,19 +277,23 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     uint8_t *sm_a = smem;
     uint8_t *sm_b = sm_a + S * C::A_BYTES;
     uint8_t *sm_sf = sm_b + S * C::B_BYTES;
-    Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(sm_sf + S * C::SF_BYTES);
+    float *sm_sc = reinterpret_cast<float *>(sm_sf + S * C::SF_BYTES);       // [S][SC_FLOATS]
+    float *sm_ps = sm_sc + S * C::SC_FLOATS;                                   // [2][PS_FLOATS]
+    Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(sm_ps + 2 * C::PS_FLOATS);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&ctl->full[s], 1);
+            // lane 0's expect_tx arrival + one cp.async-completion arrival per producer lane
+            mbar_init(&ctl->full[s], 1 + 32);
             mbar_init(&ctl->empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tfull[b], 1);
             mbar_init(&ctl->tempty[b], NUM_EPI_WARPS);
+            mbar_init(&ctl->pfull[b], 1);
             mbar_init(&ctl->vfull[b], 1);
             mbar_init(&ctl->vempty[b], 1 + NUM_EPI_WARPS);
         }
@@ -310,209 +345,216 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // grouped problems: the cp.async A rows of a stage are waited for D
-        // iterations later, so D stages of copies are in flight while the MMA
-        // may run up to S-D stages behind the producer.
-        constexpr int D = S / 2;
+        // Only asynchronous copies: TMA for the operand tiles, cp.async for the
+        // stage's fp32 scales (and, for grouped problems, the A rows, whose
+        // count lives on the device).  Each lane's cp.async completion arrives
+        // on full[s] by itself, so this warp never waits for its own copies.
         const int total = my_tiles * c.KS;
-        float pa0, pb0, pa1, pb1, pa2, pb2, pa3, pb3;
-        load_stage_scales<BN, GROUPED>(sch, 0, total, lane, pa0, pb0);
-        load_stage_scales<BN, GROUPED>(sch, 1, total, lane, pa1, pb1);
-        load_stage_scales<BN, GROUPED>(sch, 2, total, lane, pa2, pb2);
-        load_stage_scales<BN, GROUPED>(sch, 3, total, lane, pa3, pb3);
         int withheld = -1;   // slot never armed (test hook), excluded from the drain
         int it = 0;
-        bool ok = true;
         for (; it < total; ++it) {
             const int s = it % S;
             const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
-            ok = wait_bar(&ctl->empty[s], ph ^ 1u, ctl, c);
+            bool ok = wait_bar(&ctl->empty[s], ph ^ 1u, ctl, c);
             ok = __all_sync(FULL, ok);
             if (!ok) break;
+            if ((c.withhold_stage == it) && blockIdx.x == 0) {
+                withheld = s;
+                continue;
+            }
+            if (lane == 0) trace_event(c, TR_PROD_EMPTY_OK, it);
             const int ti = it / c.KS;
             const int ks = it % c.KS;
             const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + ti * static_cast<int>(gridDim.x));
+            const GroupEntry &e = sch.entry(tt.g);
             const int k0 = ks * BK;
-            const bool withhold = (c.withhold_stage == it) && blockIdx.x == 0;
-            if (withhold) {
-                withheld = s;
-            } else {
-                // full[s] counts one arrival: the transaction bytes are registered
-                // first, the arrival comes once the scale lines (and, for grouped
-                // problems, the cp.async A rows) are in shared memory.
-                if (lane == 0) {
-                    if constexpr (!GROUPED) {
-                        mbar_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
-                        tma_load_2d(&args.tmA, &ctl->full[s], sm_a + s * C::A_BYTES, k0, tt.m0);
-                        tma_load_2d(&args.tmB, &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0);
-                    } else {
-                        mbar_expect_tx(&ctl->full[s], C::B_BYTES);
-                        tma_load_2d(&args.tmB[tt.g], &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0);
-                    }
-                }
-                // scale lines for this stage (UE8M0, 32 identical 16-byte lines per chunk)
-                uint32_t wa = ue8m0_of(pa0) << (8 * (lane & 3));
-                wa |= __shfl_xor_sync(FULL, wa, 1);
-                wa |= __shfl_xor_sync(FULL, wa, 2);
-                uint32_t wb = ue8m0_of(pb0) << (8 * (lane & 3));
-                wb |= __shfl_xor_sync(FULL, wb, 1);
-                wb |= __shfl_xor_sync(FULL, wb, 2);
-                uint4 la;
-                la.x = __shfl_sync(FULL, wa, 0);
-                la.y = __shfl_sync(FULL, wa, 4);
-                la.z = __shfl_sync(FULL, wa, 8);
-                la.w = __shfl_sync(FULL, wa, 12);
-                uint8_t *sf = sm_sf + s * C::SF_BYTES;
-                *reinterpret_cast<uint4 *>(sf + lane * 16) = la;
-#pragma unroll
-                for (int q = 0; q < C::SFB_CHUNKS; ++q) {
-                    uint4 lb;
-                    lb.x = __shfl_sync(FULL, wb, 16 * q + 0);
-                    lb.y = __shfl_sync(FULL, wb, 16 * q + 4);
-                    lb.z = __shfl_sync(FULL, wb, 16 * q + 8);
-                    lb.w = __shfl_sync(FULL, wb, 16 * q + 12);
-                    *reinterpret_cast<uint4 *>(sf + 512 * (1 + q) + lane * 16) = lb;
-                }
-                if constexpr (GROUPED) {
-                    // A rows of this group: 16-byte cp.async into the swizzled layout;
-                    // chunks past K are zero-filled, rows past M_g are not loaded
-                    // (they only feed output rows that are never stored).
-                    const GroupEntry &e = sch.entry(tt.g);
-                    const int rows = min(BM, tt.Mg - tt.m0);
-                    const uint32_t dst0 = smem_u32(sm_a + s * C::A_BYTES);
-                    for (int idx = lane; idx < rows * 8; idx += 32) {
-                        const int r = idx >> 3, ch = idx & 7;
-                        const int kk = k0 + ch * 16;
-                        const bool in = kk < c.K;
-                        const uint8_t *src =
-                            e.A + static_cast<int64_t>(tt.m0 + r) * c.K + (in ? kk : 0);
-                        const uint32_t dst = dst0 + r * 128 + ((ch ^ (r & 7)) << 4);
-                        cp_async_16(dst, src, in ? 16u : 0u);
-                    }
-                    cp_async_commit();
-                }
+            if (lane == 0) {
                 if constexpr (!GROUPED) {
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->full[s]);
+                    mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
+                    tma_load_2d(&args.tmA, &ctl->full[s], sm_a + s * C::A_BYTES, k0, tt.m0);
+                    tma_load_2d(&args.tmB, &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0);
                 } else {
-                    // arrive for the stage issued D iterations ago once its copies landed
-                    cp_async_wait_group<D>();
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    const int old = it - D;
-                    if (old >= 0 && lane == 0 && (old % S) != withheld) mbar_arrive(&ctl->full[old % S]);
+                    mbar_arrive_expect_tx(&ctl->full[s], C::B_BYTES);
+                    tma_load_2d(&args.tmB[tt.g], &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0);
+                }
+            }
+            // scales of this stage: sc[rb*4 + j] = sA[m0/32 + rb][kb0 + j] (rb < 4),
+            // sc[16 + cb*4 + j] = sB[n0/32 + cb][kb0 + j] (cb < BN/32); absent
+            // blocks are zero-filled (they only meet discarded rows or K past the end)
+            {
+                const uint32_t sc = smem_u32(sm_sc + s * C::SC_FLOATS);
+                const int kb = ks * KB_PER_STAGE + (lane & 3);
+                const bool kb_ok = kb < c.KB;
+                if (lane < 16) {
+                    const int mb = tt.m0 / 32 + (lane >> 2);
+                    const bool in = kb_ok && mb < (tt.Mg + 31) / 32;
+                    const float *src = in ? e.sA + static_cast<int64_t>(mb) * c.KB + kb : e.sA;
+                    cp_async_4(sc + 4 * lane, src, in ? 4u : 0u);
+                }
+#pragma unroll
+                for (int x = lane; x < 4 * NBB; x += 32) {
+                    const int nb = tt.n0 / 32 + (x >> 2);
+                    const bool in = kb_ok && nb < c.N / 32;
+                    const float *src = in ? e.sB + static_cast<int64_t>(nb) * c.KB + kb : e.sB;
+                    cp_async_4(sc + 64 + 4 * x, src, in ? 4u : 0u);
                 }
             }
             if constexpr (GROUPED) {
-                if (withhold) {
-                    cp_async_commit();   // keep one group per iteration
-                    cp_async_wait_group<D>();
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    const int old = it - D;
-                    if (old >= 0 && lane == 0 && (old % S) != withheld) mbar_arrive(&ctl->full[old % S]);
+                // A rows of this group: 16-byte cp.async into the 128-byte swizzled
+                // layout; chunks past K are zero-filled, rows past M_g are not
+                // loaded (they only feed output rows that are never stored).
+                const int rows = min(BM, tt.Mg - tt.m0);
+                const uint32_t dst0 = smem_u32(sm_a + s * C::A_BYTES);
+                for (int idx = lane; idx < rows * 8; idx += 32) {
+                    const int r = idx >> 3, ch = idx & 7;
+                    const int kk = k0 + ch * 16;
+                    const bool in = kk < c.K;
+                    const uint8_t *src = e.A + static_cast<int64_t>(tt.m0 + r) * c.K + (in ? kk : 0);
+                    cp_async_16(dst0 + r * 128 + ((ch ^ (r & 7)) << 4), src, in ? 16u : 0u);
                 }
             }
-            pa0 = pa1; pb0 = pb1;
-            pa1 = pa2; pb1 = pb2;
-            pa2 = pa3; pb2 = pb3;
-            load_stage_scales<BN, GROUPED>(sch, it + 4, total, lane, pa3, pb3);
-        }
-        if constexpr (GROUPED) {
-            // stages whose arrive is still pending: those issued in the last S-1 iterations
-            cp_async_wait_group<0>();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                for (int old = max(0, it - D); old < it; ++old)
-                    if ((old % S) != withheld) mbar_arrive(&ctl->full[old % S]);
-            }
+            cp_async_mbar_arrive_noinc(&ctl->full[s]);
         }
         // drain: every armed stage's last phase must complete before the CTA exits
         if (lane == 0) {
             for (int d = max(0, it - S); d < it; ++d) {
                 const int s = d % S;
-                if (s == withheld && d >= it - S) continue;
+                if (s == withheld) continue;
                 wait_bar_drain(&ctl->full[s], static_cast<uint32_t>(d / S) & 1u, c.wait_limit);
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            int it = 0;
-            uint32_t u = 0;
-            bool ok = true;
-            bool issued = false;
-            for (int i = 0; i < my_tiles && ok; ++i) {
-                const int v = i & 1;
-                ok = wait_bar(&ctl->vfull[v], static_cast<uint32_t>(i >> 1) & 1u, ctl, c);
+        // ---------------------------------------------------------- MMA warp
+        // All 32 lanes follow the pipeline (they stage the scales); lane 0
+        // issues the tensor-core instructions.
+        int it = 0;
+        uint32_t u = 0;
+        bool ok = true;
+        bool issued = false;
+        for (int i = 0; i < my_tiles && ok; ++i) {
+            const int v = i & 1;
+            ok = __all_sync(FULL, wait_bar(&ctl->vfull[v], static_cast<uint32_t>(i >> 1) & 1u, ctl, c));
+            if (!ok) break;
+            const bool promote = ctl->verdict[v] != 0;
+            if (!promote) {
+                const uint32_t buf = u & 1u;
+                ok = __all_sync(FULL, wait_bar(&ctl->tempty[buf], ((u >> 1) & 1u) ^ 1u, ctl, c));
                 if (!ok) break;
-                const bool promote = ctl->verdict[v] != 0;
-                if (!promote) {
-                    const uint32_t buf = u & 1u;
-                    ok = wait_bar(&ctl->tempty[buf], ((u >> 1) & 1u) ^ 1u, ctl, c);
+                if (lane == 0) trace_event(c, TR_MMA_BUF_OK, static_cast<int>(u));
+                tc_fence_after();
+                const uint32_t d = tmem + buf * BN;
+                for (int ks = 0; ks < c.KS; ++ks, ++it) {
+                    const int s = it % S;
+                    ok = __all_sync(FULL, wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c));
                     if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t d = tmem + buf * BN;
-                    for (int ks = 0; ks < c.KS; ++ks, ++it) {
-                        const int s = it % S;
-                        ok = wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c);
-                        if (!ok) break;
+                    if (lane == 0) trace_event(c, TR_MMA_FULL_OK, it);
+                    // UE8M0 scale lines for tcgen05.cp: 32 identical 16-byte lines per
+                    // 128 rows; word w of a line = row block w, byte j = K block j.
+                    const float *sc = sm_sc + s * C::SC_FLOATS;
+                    const float va = lane < 16 ? sc[lane] : 1.0f;
+                    const float vb = lane < 4 * NBB ? sc[16 + lane] : 1.0f;
+                    uint32_t wa = ue8m0_of(va) << (8 * (lane & 3));
+                    wa |= __shfl_xor_sync(FULL, wa, 1);
+                    wa |= __shfl_xor_sync(FULL, wa, 2);
+                    uint32_t wb = ue8m0_of(vb) << (8 * (lane & 3));
+                    wb |= __shfl_xor_sync(FULL, wb, 1);
+                    wb |= __shfl_xor_sync(FULL, wb, 2);
+                    uint8_t *sf = sm_sf + s * C::SF_BYTES;
+                    uint4 la;
+                    la.x = __shfl_sync(FULL, wa, 0);
+                    la.y = __shfl_sync(FULL, wa, 4);
+                    la.z = __shfl_sync(FULL, wa, 8);
+                    la.w = __shfl_sync(FULL, wa, 12);
+                    *reinterpret_cast<uint4 *>(sf + lane * 16) = la;
+#pragma unroll
+                    for (int q = 0; q < C::SFB_CHUNKS; ++q) {
+                        uint4 lb;
+                        lb.x = __shfl_sync(FULL, wb, 16 * q + 0);
+                        lb.y = __shfl_sync(FULL, wb, 16 * q + 4);
+                        lb.z = __shfl_sync(FULL, wb, 16 * q + 8);
+                        lb.w = __shfl_sync(FULL, wb, 16 * q + 12);
+                        *reinterpret_cast<uint4 *>(sf + 512 * (1 + q) + lane * 16) = lb;
+                    }
+                    // the lines (and grouped A rows written by cp.async) become
+                    // visible to the tensor core's async-proxy reads
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        trace_event(c, TR_MMA_LINES, it);
                         tc_fence_after();
                         const uint32_t sfa = tmem + C::SF_COL0 + s * C::SF_COLS;
                         const uint32_t sfb = sfa + 4;
-                        const uint32_t sf_s = smem_u32(sm_sf + s * C::SF_BYTES);
+                        const uint32_t sf_s = smem_u32(sf);
                         tmem_cp_32x128b_warpx4(sfa, sdesc_sf_lines(sf_s));
 #pragma unroll
                         for (int q = 0; q < C::SFB_CHUNKS; ++q)
                             tmem_cp_32x128b_warpx4(sfb + 4 * q, sdesc_sf_lines(sf_s + 512 * (1 + q)));
+                        trace_event(c, TR_MMA_CP, it);
                         const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
                         const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
                         const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
-                        issued = true;
                         for (int j = 0; j < nk; ++j) {
                             mma_mxf8(d, ad + static_cast<uint64_t>(2 * j), bd + static_cast<uint64_t>(2 * j),
-                                     idesc_mxf8f6f4(BM, BN, j, j), sfa, sfb,
-                                     (ks | j) != 0 ? 1u : 0u);
+                                     idesc_mxf8f6f4(BM, BN, j, j), sfa, sfb, (ks | j) != 0 ? 1u : 0u);
                         }
+                        trace_event(c, TR_MMA_MMA, it);
                         mma_commit(&ctl->empty[s]);
+                        trace_event(c, TR_MMA_ISSUED, it);
                     }
+                    issued = true;
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (lane == 0) mma_commit(&ctl->tfull[buf]);
+                ++u;
+            } else {
+                for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
+                    const int s = it % S;
+                    ok = __all_sync(FULL, wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c));
                     if (!ok) break;
-                    mma_commit(&ctl->tfull[buf]);
-                    ++u;
-                } else {
-                    for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
-                        const int s = it % S;
-                        ok = wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c);
+                    if (lane == 0) trace_event(c, TR_MMA_FULL_OK, it);
+                    fence_proxy_async_smem();   // grouped A rows written by cp.async
+                    const float *sc = sm_sc + s * C::SC_FLOATS;
+                    const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
+                    const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
+                    const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
+                    for (int j = 0; j < nk; ++j) {
+                        const uint32_t buf = u & 1u;
+                        ok = __all_sync(FULL, wait_bar(&ctl->tempty[buf], ((u >> 1) & 1u) ^ 1u, ctl, c));
                         if (!ok) break;
-                        tc_fence_after();
-                        const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
-                        const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
-                        const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
-                        for (int j = 0; j < nk; ++j) {
-                            const uint32_t buf = u & 1u;
-                            ok = wait_bar(&ctl->tempty[buf], ((u >> 1) & 1u) ^ 1u, ctl, c);
-                            if (!ok) break;
+                        if (lane == 0) trace_event(c, TR_MMA_BUF_OK, static_cast<int>(u));
+                        // scale products of this K block: ps[rb*NBB + cb] = sA[rb]*sB[cb]
+                        if (lane < 4 * NBB) {
+                            const int rb = lane / NBB, cb = lane % NBB;
+                            sm_ps[buf * C::PS_FLOATS + lane] = sc[rb * 4 + j] * sc[16 + cb * 4 + j];
+                        }
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(&ctl->pfull[buf]);
                             tc_fence_after();
-                            issued = true;
                             mma_f8(tmem + buf * BN, ad + static_cast<uint64_t>(2 * j),
                                    bd + static_cast<uint64_t>(2 * j), idesc_f8f6f4(BM, BN), 0u);
                             mma_commit(&ctl->tfull[buf]);
-                            ++u;
                         }
-                        if (!ok) break;
-                        mma_commit(&ctl->empty[s]);
+                        issued = true;
+                        ++u;
                     }
                     if (!ok) break;
+                    if (lane == 0) {
+                        mma_commit(&ctl->empty[s]);
+                        trace_event(c, TR_MMA_ISSUED, it);
+                    }
+                    __syncwarp();
                 }
-                mbar_arrive(&ctl->vempty[v]);
+                if (!ok) break;
             }
-            // all issued tensor-core work must finish before tensor memory is freed
-            if (issued) {
-                mma_commit(&ctl->drain);
-                wait_bar_drain(&ctl->drain, 0u, c.wait_limit);
-            }
+            if (lane == 0) mbar_arrive(&ctl->vempty[v]);
+            __syncwarp();
+        }
+        // all issued tensor-core work must finish before tensor memory is freed
+        if (issued && lane == 0) {
+            mma_commit(&ctl->drain);
+            wait_bar_drain(&ctl->drain, 0u, c.wait_limit);
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -537,13 +579,13 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 const int nbn = (nb1 - nb0) * c.KB;
                 for (int x = lane; x < na; x += 32 * 8) {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (x + 32 * u < na) bad |= !is_pow2_scale(__ldg(pa + x + 32 * u));
+                    for (int w = 0; w < 8; ++w)
+                        if (x + 32 * w < na) bad |= !is_pow2_scale(__ldg(pa + x + 32 * w));
                 }
                 for (int x = lane; x < nbn; x += 32 * 8) {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (x + 32 * u < nbn) bad |= !is_pow2_scale(__ldg(pb + x + 32 * u));
+                    for (int w = 0; w < 8; ++w)
+                        if (x + 32 * w < nbn) bad |= !is_pow2_scale(__ldg(pb + x + 32 * w));
                 }
                 const bool any_bad = __any_sync(FULL, bad);
                 verdict = any_bad ? 1 : 0;
@@ -552,6 +594,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             if (lane == 0) {
                 ctl->verdict[v] = verdict;
                 mbar_arrive(&ctl->vfull[v]);
+                trace_event(c, TR_VERDICT, i);
             }
             __syncwarp();
         }
@@ -579,6 +622,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 ok = wait_bar(&ctl->tfull[buf], (u >> 1) & 1u, ctl, c);
                 ok = __all_sync(FULL, ok);
                 if (!ok) break;
+                if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_FULL_OK, static_cast<int>(u));
                 tc_fence_after();
 #pragma unroll 1
                 for (int ch = 0; ch < C::EPI_COLS / 32; ++ch) {
@@ -590,23 +634,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+                        if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_RELEASED, static_cast<int>(u));
                     }
-                    if (row_ok && tt.n0 + col < c.N) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            uint4 o;
-                            __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(r[8 * w + 0]), __uint_as_float(r[8 * w + 1]));
-                            __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(r[8 * w + 2]), __uint_as_float(r[8 * w + 3]));
-                            __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(r[8 * w + 4]), __uint_as_float(r[8 * w + 5]));
-                            __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(r[8 * w + 6]), __uint_as_float(r[8 * w + 7]));
-                            o.x = *reinterpret_cast<uint32_t *>(&p0);
-                            o.y = *reinterpret_cast<uint32_t *>(&p1);
-                            o.z = *reinterpret_cast<uint32_t *>(&p2);
-                            o.w = *reinterpret_cast<uint32_t *>(&p3);
-                            dst[w] = o;
-                        }
-                    }
+                    if (row_ok && tt.n0 + col < c.N) store_bf16x32(crow + col, r);
                 }
                 ++u;
             } else {
@@ -614,25 +644,17 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 float acc[C::EPI_COLS];
 #pragma unroll
                 for (int x = 0; x < C::EPI_COLS; ++x) acc[x] = 0.0f;
-                const int MB = (tt.Mg + 31) / 32;
-                const int mb = tt.m0 / 32 + q;
-                const bool mb_ok = mb < MB;
-                const float *sa_row = e.sA + static_cast<int64_t>(mb_ok ? mb : 0) * c.KB;
-                const float *sb_row = e.sB + static_cast<int64_t>((tt.n0 + col0) / 32) * c.KB;
-                int nb_valid = (c.N - (tt.n0 + col0)) / 32;   // column blocks of this warp inside N
-                nb_valid = nb_valid < 0 ? 0 : (nb_valid > NCH ? NCH : nb_valid);
                 for (int kb = 0; kb < c.KB; ++kb) {
-                    // scale products for this K block (the same for all lanes)
-                    const float sa = mb_ok ? __ldg(sa_row + kb) : 0.0f;
-                    float sc[NCH];
-#pragma unroll
-                    for (int x = 0; x < NCH; ++x)
-                        sc[x] = (x < nb_valid) ? sa * __ldg(sb_row + static_cast<int64_t>(x) * c.KB + kb) : 0.0f;
                     const uint32_t buf = u & 1u;
-                    ok = wait_bar(&ctl->tfull[buf], (u >> 1) & 1u, ctl, c);
+                    ok = wait_bar(&ctl->pfull[buf], (u >> 1) & 1u, ctl, c) &&
+                         wait_bar(&ctl->tfull[buf], (u >> 1) & 1u, ctl, c);
                     ok = __all_sync(FULL, ok);
                     if (!ok) break;
+                    if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_FULL_OK, static_cast<int>(u));
                     tc_fence_after();
+                    float sc[NCH];
+#pragma unroll
+                    for (int x = 0; x < NCH; ++x) sc[x] = sm_ps[buf * C::PS_FLOATS + q * NBB + h * NCH + x];
                     uint32_t r[NCH][32];
 #pragma unroll
                     for (int x = 0; x < NCH; ++x) tmem_ld_x32(tmem + lane_base + buf * BN + col0 + 32 * x, r[x]);
@@ -640,6 +662,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+                    if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_RELEASED, static_cast<int>(u));
                     ++u;
 #pragma unroll
                     for (int x = 0; x < NCH; ++x)
@@ -652,21 +675,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 #pragma unroll
                     for (int x = 0; x < NCH; ++x) {
                         const int col = col0 + 32 * x;
-                        if (tt.n0 + col >= c.N) continue;
-                        uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            uint4 o;
-                            __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[32 * x + 8 * w + 0], acc[32 * x + 8 * w + 1]);
-                            __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[32 * x + 8 * w + 2], acc[32 * x + 8 * w + 3]);
-                            __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[32 * x + 8 * w + 4], acc[32 * x + 8 * w + 5]);
-                            __nv_bfloat162 p3 = __floats2bfloat162_rn(acc[32 * x + 8 * w + 6], acc[32 * x + 8 * w + 7]);
-                            o.x = *reinterpret_cast<uint32_t *>(&p0);
-                            o.y = *reinterpret_cast<uint32_t *>(&p1);
-                            o.z = *reinterpret_cast<uint32_t *>(&p2);
-                            o.w = *reinterpret_cast<uint32_t *>(&p3);
-                            dst[w] = o;
-                        }
+                        if (tt.n0 + col < c.N) store_bf16x32f(crow + col, acc + 32 * x);
                     }
                 }
             }

@@ -63,6 +63,13 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
 }
 
 // ------------------------------------------------------------- cp.async ----
+// 4-byte global->shared copy (L1-cached); src_bytes == 0 writes 4 zero bytes.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
 // 16-byte global->shared copy; src_bytes == 0 writes 16 zero bytes.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
