@@ -91,7 +91,7 @@ int device_setup(DeviceState **out) {
             return FP8_ERR_CUDA;
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    int rc = set_kernel_attrs<128>();
+    int rc = set_kernel_attrs<TILE_N>();
     if (rc != FP8_OK) return rc;
     if (!d.status) {
         if (cudaMalloc(&d.status, 256) != cudaSuccess) return FP8_ERR_CUDA;
@@ -241,7 +241,7 @@ int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const
     rc = device_setup(&d);
     if (rc != FP8_OK) return rc;
     if (K == 0) return zero_fill(C, M * N, stream);
-    return launch_plain<128>(A, sA, B, sB, C, M, N, K, mode, d, stream);
+    return launch_plain<TILE_N>(A, sA, B, sB, C, M, N, K, mode, d, stream);
 }
 
 int fp8_gemm_blockscaled(const void *A, const float *sA, const void *B, const float *sB, void *C,
@@ -272,7 +272,7 @@ int fp8_gemm_grouped_ex(const fp8_group_desc *groups, const int32_t *Ms, int64_t
     if (K == 0) return FP8_ERR_SHAPE;   // row counts are on the device: no host-side zero fill
     for (int32_t g0 = 0; g0 < G; g0 += FP8_MAX_GROUPS_PER_LAUNCH) {
         const int32_t n = (G - g0) < FP8_MAX_GROUPS_PER_LAUNCH ? (G - g0) : FP8_MAX_GROUPS_PER_LAUNCH;
-        rc = launch_grouped<128>(groups + g0, Ms + g0, N, K, n, mode, d, stream);
+        rc = launch_grouped<TILE_N>(groups + g0, Ms + g0, N, K, n, mode, d, stream);
         if (rc != FP8_OK) return rc;
     }
     return FP8_OK;

@@ -1,5 +1,5 @@
 // gemm_kernel.cuh -- persistent, warp-specialised block-scaled E4M3 GEMM for
-// sm_103a (tcgen05 tensor cores, tensor memory accumulators, TMA).
+// sm_103a (tcgen05 tensor cores, tensor-memory accumulators, TMA).
 //
 // Computes C[m,n] = bf16( sum_kb sA[m/32][kb] * sB[n/32][kb] * sum_{k in kb}
 // A[m,k] B[n,k] ) (FP8 GEMM library article, hncyxsy.com/news/241433,
@@ -7,27 +7,46 @@
 // for one problem or for a group of independent problems (same article,
 // section 4.2: one launch, each block looks up its problem in a table).
 //
+// Output tile: 128 rows x BN (256) columns; one tcgen05.mma is M=128, N=BN,
+// K=32 (one 32-K scale block).  On this part an M=128 MMA costs ~116 cycles for
+// any N <= 128 but only ~140-165 for N = 256, so N = 256 is what reaches the
+// tensor peak.  The MMA issue blocks until the previous MMA retires, so the
+// issuing thread does nothing else.
+//
 // Roles (384 threads, one CTA per SM, persistent over output tiles):
 //   warp 0     producer: TMA loads of the A and B K-slices into a ring of
-//              shared-memory stages (128-byte swizzle; for grouped problems A
-//              rows come by cp.async since the row counts live on the device),
-//              plus the stage's scale lines: the 32x32 block scales of the
-//              tile converted to UE8M0 bytes in the layout tcgen05.cp wants.
-//   warp 1     MMA issuer (one thread): native path = tcgen05.mma
-//              kind::mxf8f6f4 with the UE8M0 scales copied into tensor memory;
-//              promotion path = one unscaled kind::f8f6f4 MMA per 32-K block
-//              into a fresh tensor-memory partial.
+//              shared-memory stages (128-byte swizzle; for grouped problems the
+//              A rows come by cp.async since their count lives on the device),
+//              and cp.async of the stage's fp32 block scales.  Only
+//              asynchronous copies: each lane's cp.async completion arrives on
+//              the stage barrier by itself.
+//   warp 1     MMA issuer.  Native path: lane 0 copies the stage's UE8M0 scale
+//              lines into tensor memory (tcgen05.cp) and issues the four
+//              kind::mxf8f6f4 block-scaled MMAs into the accumulator.
+//              Promotion path: the warp publishes the K block's scale products
+//              and lane 0 issues one unscaled kind::f8f6f4 MMA per 32-K block
+//              into one of two tensor-memory partials.
 //   warp 2     path verdict: scans each tile's scales one or two tiles ahead
 //              and decides native (all positive normal powers of two) or
 //              promotion.
-//   warps 4-11 epilogue: tensor memory -> registers -> bf16 -> global
-//              (native); or per-32-K-block promotion acc += sA*sB*partial in
-//              fp32 registers, then bf16 -> global.
+//   warp 3     scale warp: turns each stage's fp32 scales into the 32
+//              identical 16-byte UE8M0 lines per 128 rows that tcgen05.cp
+//              replicates into all lane quarters, then releases the stage to
+//              the MMA warp.
+//   warps 4-11 epilogue: native tiles drain the accumulator into registers,
+//              release it to the MMA warp at once, then convert to bf16 and
+//              store; promotion tiles accumulate acc += (sA*sB) * partial per
+//              32-K block in fp32 registers and store at the end.
 //
 // The K loop of every tile runs whole and in ascending K order, with a tile
-// shape that depends only on (N, grouped or not): no split-K, no stream-K, so
-// each output row is independent of M and of the other rows ("AI Infra
+// shape that depends only on the kernel, never on M: no split-K, no stream-K,
+// so each output row is independent of M and of the other rows ("AI Infra
 // 进阶：如何让大模型输出确定的结果", aif.amtbbs.org post 29992, section 1).
+//
+// Tensor memory (512 columns): accumulator / partial 0 at [0, BN), partial 1
+// at [BN, 2 BN), the per-stage scale columns at [SF_COL0, ...).  For BN = 256
+// the scale columns share partial 1's range; path changes between tiles wait
+// for both buffers to drain first.
 //
 // Every wait is bounded (clock64 budget).  On expiry a CTA-wide abort flag
 // and the device status word are set, every role leaves its loop, in-flight
@@ -49,6 +68,7 @@ constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int MAX_GROUPS = 64;
 constexpr int GROUP_M = 8;         // tile-order swizzle width (m-tiles) for L2 reuse
+constexpr int TILE_N = 256;        // the BN every launch uses
 
 enum : uint32_t { STATUS_TIMEOUT = 1u, STATUS_SCALE = 2u };
 enum : int { PATH_AUTO = 0, PATH_NATIVE = 1, PATH_PROMOTE = 2 };
@@ -62,15 +82,15 @@ struct Cfg {
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;           // 128 B rows per tcgen05.cp
     static constexpr int SF_BYTES = 512 * (1 + SFB_CHUNKS);         // scale lines per stage
     static constexpr int SF_COLS = 4 * (1 + SFB_CHUNKS);            // tensor-memory columns per stage
-    static constexpr int ACC_COLS = 2 * BN;                         // two accumulator / partial buffers
-    static constexpr int SF_COL0 = ACC_COLS;
-    static constexpr int TMEM_USED = ACC_COLS + STAGES * SF_COLS;
-    static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
+    static constexpr int SF_COL0 = (2 * BN + STAGES * SF_COLS <= 512) ? 2 * BN : BN;
+    static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_COLS = BN / 2;                         // columns per epilogue warp
-    static constexpr int SC_FLOATS = 64;                            // staged fp32 scales per stage: 16 A + up to 32 B
-    static constexpr int PS_FLOATS = 4 * (BN / 32);                 // scale products per K block (promotion)
-    static_assert(TMEM_USED <= 512, "tensor memory budget");
+    static constexpr int NBB = BN / 32;                             // 32-column blocks per tile
+    static constexpr int SC_FLOATS = 16 + 4 * NBB;                  // staged fp32 scales per stage
+    static constexpr int PS_FLOATS = 4 * NBB;                       // scale products per K block
+    static_assert(SF_COL0 + STAGES * SF_COLS <= 512 && SF_COL0 >= BN, "tensor memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
+    static_assert(4 * NBB <= 32, "one scale product per MMA-warp lane");
 };
 
 struct GroupEntry {
@@ -96,16 +116,16 @@ struct Common {
 // SM clock of pipeline events into trace[event * TRACE_SLOTS + index].
 constexpr int TRACE_SLOTS = 1024;
 enum : int {
-    TR_PROD_EMPTY_OK = 0,   // producer: slot free, about to issue stage `it`
-    TR_MMA_FULL_OK = 1,     // MMA warp: stage `it` landed
-    TR_MMA_ISSUED = 2,      // MMA warp: stage `it` MMAs issued and committed
-    TR_EPI_FULL_OK = 3,     // epilogue warp 4: accumulator / partial `u` ready
-    TR_EPI_RELEASED = 4,    // epilogue warp 4: accumulator / partial `u` released
-    TR_MMA_BUF_OK = 5,      // MMA warp: buffer `u` free
-    TR_VERDICT = 6,         // verdict warp: tile `i` published
-    TR_MMA_LINES = 7,       // MMA warp: scale lines of stage `it` written and fenced
-    TR_MMA_CP = 8,          // MMA warp: scale copies of stage `it` issued
-    TR_MMA_MMA = 9,         // MMA warp: MMAs of stage `it` issued (before the commit)
+    TR_PROD_ISSUE = 0,      // producer: slot free, issuing stage `it`
+    TR_SCALE_FULL = 1,      // scale warp: stage `it` landed
+    TR_SCALE_READY = 2,     // scale warp: stage `it` lines written, released
+    TR_MMA_READY = 3,       // MMA lane 0: stage `it` available
+    TR_MMA_ISSUED = 4,      // MMA lane 0: stage `it` MMAs issued and committed
+    TR_EPI_FULL = 5,        // epilogue warp 4: accumulator of tile `i` ready
+    TR_EPI_RELEASED = 6,    // epilogue warp 4: accumulator of tile `i` released
+    TR_EPI_STORED = 7,      // epilogue warp 4: tile `i` stored
+    TR_VERDICT = 8,         // verdict warp: tile `i` published
+    TR_MMA_TILE = 9,        // MMA lane 0: tile `i` accumulator free, starting
     TR_EVENTS = 10
 };
 
@@ -129,12 +149,13 @@ struct GroupedArgs {
 
 template <int STAGES>
 struct Ctrl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
-    uint64_t pfull[2];
-    uint64_t vfull[2];
+    uint64_t full[STAGES];      // producer -> scale warp (TMA bytes + cp.async arrivals)
+    uint64_t sfready[STAGES];   // scale warp -> MMA warp
+    uint64_t empty[STAGES];     // MMA commit -> producer
+    uint64_t tfull[2];          // MMA commit -> epilogue (accumulator / partial b)
+    uint64_t tempty[2];         // epilogue -> MMA
+    uint64_t pfull[2];          // MMA warp -> epilogue (scale products of partial b)
+    uint64_t vfull[2];          // verdict -> MMA, scale and epilogue warps
     uint64_t vempty[2];
     uint64_t drain;
     uint32_t tmem_base;
@@ -188,6 +209,8 @@ __device__ __forceinline__ bool is_pow2_scale(float v) {
     return (b & 0x007FFFFFu) == 0u && e != 0u && e < 255u;
 }
 
+__device__ __forceinline__ uint32_t ue8m0_of(float v) { return (__float_as_uint(v) >> 23) & 0xFFu; }
+
 template <int BN, bool GROUPED, typename Args>
 struct Sched {
     const Args &a;
@@ -232,7 +255,7 @@ struct Sched {
 };
 
 // 32 consecutive bf16 outputs (64 bytes, 16-byte aligned) from fp32 bits / values.
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t *r) {
     uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
@@ -261,14 +284,12 @@ __device__ __forceinline__ void store_bf16x32f(__nv_bfloat16 *dst, const float *
     }
 }
 
-__device__ __forceinline__ uint32_t ue8m0_of(float v) { return (__float_as_uint(v) >> 23) & 0xFFu; }
-
 // ---------------------------------------------------------------------------
 template <int BN, bool GROUPED, typename Args>
 __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     using C = Cfg<BN>;
     constexpr int S = C::STAGES;
-    constexpr int NBB = BN / 32;          // column blocks of B per tile
+    constexpr int NBB = C::NBB;
     constexpr uint32_t FULL = 0xFFFFFFFFu;
     const Common &c = args.c;
 
@@ -288,6 +309,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         for (int s = 0; s < S; ++s) {
             // lane 0's expect_tx arrival + one cp.async-completion arrival per producer lane
             mbar_init(&ctl->full[s], 1 + 32);
+            mbar_init(&ctl->sfready[s], 1);
             mbar_init(&ctl->empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -295,7 +317,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             mbar_init(&ctl->tempty[b], NUM_EPI_WARPS);
             mbar_init(&ctl->pfull[b], 1);
             mbar_init(&ctl->vfull[b], 1);
-            mbar_init(&ctl->vempty[b], 1 + NUM_EPI_WARPS);
+            mbar_init(&ctl->vempty[b], 2 + NUM_EPI_WARPS);   // MMA + scale warp + epilogue
         }
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
@@ -345,10 +367,6 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // Only asynchronous copies: TMA for the operand tiles, cp.async for the
-        // stage's fp32 scales (and, for grouped problems, the A rows, whose
-        // count lives on the device).  Each lane's cp.async completion arrives
-        // on full[s] by itself, so this warp never waits for its own copies.
         const int total = my_tiles * c.KS;
         int withheld = -1;   // slot never armed (test hook), excluded from the drain
         int it = 0;
@@ -362,7 +380,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 withheld = s;
                 continue;
             }
-            if (lane == 0) trace_event(c, TR_PROD_EMPTY_OK, it);
+            if (lane == 0) trace_event(c, TR_PROD_ISSUE, it);
             const int ti = it / c.KS;
             const int ks = it % c.KS;
             const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + ti * static_cast<int>(gridDim.x));
@@ -425,10 +443,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA warp
-        // All 32 lanes follow the pipeline (they stage the scales); lane 0
-        // issues the tensor-core instructions.
-        int it = 0;
-        uint32_t u = 0;
+        int it = 0;                       // stage counter (same sequence as the producer)
+        uint32_t uses0 = 0, uses1 = 0;    // completed uses of tensor-memory buffers 0 / 1
+        uint32_t pk = 0;                  // promotion partials issued (buffer = pk & 1)
+        uint32_t pu0 = 0, pu1 = 0;        // promotion uses of buffers 0 / 1 (pfull phases)
         bool ok = true;
         bool issued = false;
         for (int i = 0; i < my_tiles && ok; ++i) {
@@ -437,113 +455,81 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             if (!ok) break;
             const bool promote = ctl->verdict[v] != 0;
             if (!promote) {
-                const uint32_t buf = u & 1u;
-                ok = __all_sync(FULL, wait_bar(&ctl->tempty[buf], ((u >> 1) & 1u) ^ 1u, ctl, c));
-                if (!ok) break;
-                if (lane == 0) trace_event(c, TR_MMA_BUF_OK, static_cast<int>(u));
-                tc_fence_after();
-                const uint32_t d = tmem + buf * BN;
-                for (int ks = 0; ks < c.KS; ++ks, ++it) {
-                    const int s = it % S;
-                    ok = __all_sync(FULL, wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c));
-                    if (!ok) break;
-                    if (lane == 0) trace_event(c, TR_MMA_FULL_OK, it);
-                    // UE8M0 scale lines for tcgen05.cp: 32 identical 16-byte lines per
-                    // 128 rows; word w of a line = row block w, byte j = K block j.
-                    const float *sc = sm_sc + s * C::SC_FLOATS;
-                    const float va = lane < 16 ? sc[lane] : 1.0f;
-                    const float vb = lane < 4 * NBB ? sc[16 + lane] : 1.0f;
-                    uint32_t wa = ue8m0_of(va) << (8 * (lane & 3));
-                    wa |= __shfl_xor_sync(FULL, wa, 1);
-                    wa |= __shfl_xor_sync(FULL, wa, 2);
-                    uint32_t wb = ue8m0_of(vb) << (8 * (lane & 3));
-                    wb |= __shfl_xor_sync(FULL, wb, 1);
-                    wb |= __shfl_xor_sync(FULL, wb, 2);
-                    uint8_t *sf = sm_sf + s * C::SF_BYTES;
-                    uint4 la;
-                    la.x = __shfl_sync(FULL, wa, 0);
-                    la.y = __shfl_sync(FULL, wa, 4);
-                    la.z = __shfl_sync(FULL, wa, 8);
-                    la.w = __shfl_sync(FULL, wa, 12);
-                    *reinterpret_cast<uint4 *>(sf + lane * 16) = la;
-#pragma unroll
-                    for (int q = 0; q < C::SFB_CHUNKS; ++q) {
-                        uint4 lb;
-                        lb.x = __shfl_sync(FULL, wb, 16 * q + 0);
-                        lb.y = __shfl_sync(FULL, wb, 16 * q + 4);
-                        lb.z = __shfl_sync(FULL, wb, 16 * q + 8);
-                        lb.w = __shfl_sync(FULL, wb, 16 * q + 12);
-                        *reinterpret_cast<uint4 *>(sf + 512 * (1 + q) + lane * 16) = lb;
-                    }
-                    // the lines (and grouped A rows written by cp.async) become
-                    // visible to the tensor core's async-proxy reads
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        trace_event(c, TR_MMA_LINES, it);
+                if (lane == 0) {
+                    // the accumulator (buffer 0) and, since the scale columns
+                    // share its range, buffer 1 must both be drained
+                    ok = wait_bar(&ctl->tempty[0], (uses0 & 1u) ^ 1u, ctl, c) &&
+                         wait_bar(&ctl->tempty[1], (uses1 & 1u) ^ 1u, ctl, c);
+                    trace_event(c, TR_MMA_TILE, i);
+                    tc_fence_after();
+                    const uint32_t sfa_base = tmem + C::SF_COL0;
+                    for (int ks = 0; ks < c.KS && ok; ++ks) {
+                        const int s = (it + ks) % S;
+                        ok = wait_bar(&ctl->sfready[s], static_cast<uint32_t>((it + ks) / S) & 1u, ctl, c);
+                        if (!ok) break;
+                        trace_event(c, TR_MMA_READY, it + ks);
                         tc_fence_after();
-                        const uint32_t sfa = tmem + C::SF_COL0 + s * C::SF_COLS;
+                        const uint32_t sfa = sfa_base + s * C::SF_COLS;
                         const uint32_t sfb = sfa + 4;
-                        const uint32_t sf_s = smem_u32(sf);
+                        const uint32_t sf_s = smem_u32(sm_sf + s * C::SF_BYTES);
                         tmem_cp_32x128b_warpx4(sfa, sdesc_sf_lines(sf_s));
 #pragma unroll
                         for (int q = 0; q < C::SFB_CHUNKS; ++q)
                             tmem_cp_32x128b_warpx4(sfb + 4 * q, sdesc_sf_lines(sf_s + 512 * (1 + q)));
-                        trace_event(c, TR_MMA_CP, it);
                         const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
                         const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
                         const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
-                        for (int j = 0; j < nk; ++j) {
-                            mma_mxf8(d, ad + static_cast<uint64_t>(2 * j), bd + static_cast<uint64_t>(2 * j),
-                                     idesc_mxf8f6f4(BM, BN, j, j), sfa, sfb, (ks | j) != 0 ? 1u : 0u);
+#pragma unroll
+                        for (int j = 0; j < KB_PER_STAGE; ++j) {
+                            if (j < nk)
+                                mma_mxf8(tmem, ad + static_cast<uint64_t>(2 * j), bd + static_cast<uint64_t>(2 * j),
+                                         idesc_mxf8f6f4(BM, BN, j, j), sfa, sfb, (ks | j) != 0 ? 1u : 0u);
                         }
-                        trace_event(c, TR_MMA_MMA, it);
                         mma_commit(&ctl->empty[s]);
-                        trace_event(c, TR_MMA_ISSUED, it);
+                        trace_event(c, TR_MMA_ISSUED, it + ks);
+                        issued = true;
                     }
-                    issued = true;
-                    __syncwarp();
+                    if (ok) mma_commit(&ctl->tfull[0]);
                 }
+                ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                issued = __shfl_sync(FULL, issued ? 1 : 0, 0) != 0;
                 if (!ok) break;
-                if (lane == 0) mma_commit(&ctl->tfull[buf]);
-                ++u;
+                it += c.KS;
+                ++uses0;
             } else {
+                if (pk & 1u) ++pk;   // promotion tiles start on buffer 0 (see the header)
                 for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
                     const int s = it % S;
-                    ok = __all_sync(FULL, wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c));
+                    ok = __all_sync(FULL, wait_bar(&ctl->sfready[s], static_cast<uint32_t>(it / S) & 1u, ctl, c));
                     if (!ok) break;
-                    if (lane == 0) trace_event(c, TR_MMA_FULL_OK, it);
-                    fence_proxy_async_smem();   // grouped A rows written by cp.async
                     const float *sc = sm_sc + s * C::SC_FLOATS;
                     const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
                     const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
                     const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
                     for (int j = 0; j < nk; ++j) {
-                        const uint32_t buf = u & 1u;
-                        ok = __all_sync(FULL, wait_bar(&ctl->tempty[buf], ((u >> 1) & 1u) ^ 1u, ctl, c));
+                        const uint32_t b = pk & 1u;
+                        const uint32_t ub = b ? uses1 : uses0;
+                        ok = __all_sync(FULL, wait_bar(&ctl->tempty[b], (ub & 1u) ^ 1u, ctl, c));
                         if (!ok) break;
-                        if (lane == 0) trace_event(c, TR_MMA_BUF_OK, static_cast<int>(u));
                         // scale products of this K block: ps[rb*NBB + cb] = sA[rb]*sB[cb]
                         if (lane < 4 * NBB) {
                             const int rb = lane / NBB, cb = lane % NBB;
-                            sm_ps[buf * C::PS_FLOATS + lane] = sc[rb * 4 + j] * sc[16 + cb * 4 + j];
+                            sm_ps[b * C::PS_FLOATS + lane] = sc[rb * 4 + j] * sc[16 + cb * 4 + j];
                         }
                         __syncwarp();
                         if (lane == 0) {
-                            mbar_arrive(&ctl->pfull[buf]);
+                            mbar_arrive(&ctl->pfull[b]);
                             tc_fence_after();
-                            mma_f8(tmem + buf * BN, ad + static_cast<uint64_t>(2 * j),
+                            mma_f8(tmem + b * BN, ad + static_cast<uint64_t>(2 * j),
                                    bd + static_cast<uint64_t>(2 * j), idesc_f8f6f4(BM, BN), 0u);
-                            mma_commit(&ctl->tfull[buf]);
+                            mma_commit(&ctl->tfull[b]);
                         }
                         issued = true;
-                        ++u;
+                        if (b) { ++uses1; ++pu1; } else { ++uses0; ++pu0; }
+                        ++pk;
                     }
                     if (!ok) break;
-                    if (lane == 0) {
-                        mma_commit(&ctl->empty[s]);
-                        trace_event(c, TR_MMA_ISSUED, it);
-                    }
+                    if (lane == 0) mma_commit(&ctl->empty[s]);
                     __syncwarp();
                 }
                 if (!ok) break;
@@ -598,12 +584,70 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             }
             __syncwarp();
         }
+    } else if (warp == 3) {
+        // --------------------------------------------------------- scale warp
+        int it = 0;
+        bool ok = true;
+        for (int i = 0; i < my_tiles && ok; ++i) {
+            const int v = i & 1;
+            ok = __all_sync(FULL, wait_bar(&ctl->vfull[v], static_cast<uint32_t>(i >> 1) & 1u, ctl, c));
+            if (!ok) break;
+            const bool promote = ctl->verdict[v] != 0;
+            for (int ks = 0; ks < c.KS; ++ks, ++it) {
+                const int s = it % S;
+                ok = __all_sync(FULL, wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c));
+                if (!ok) break;
+                if (lane == 0) trace_event(c, TR_SCALE_FULL, it);
+                if (!promote) {
+                    // UE8M0 lines for tcgen05.cp: 32 identical 16-byte lines per 128
+                    // rows; word w of a line = row block w, byte j = K block j.
+                    const float *sc = sm_sc + s * C::SC_FLOATS;
+                    const float va = lane < 16 ? sc[lane] : 1.0f;
+                    const float vb = lane < 4 * NBB ? sc[16 + lane] : 1.0f;
+                    uint32_t wa = ue8m0_of(va) << (8 * (lane & 3));
+                    wa |= __shfl_xor_sync(FULL, wa, 1);
+                    wa |= __shfl_xor_sync(FULL, wa, 2);
+                    uint32_t wb = ue8m0_of(vb) << (8 * (lane & 3));
+                    wb |= __shfl_xor_sync(FULL, wb, 1);
+                    wb |= __shfl_xor_sync(FULL, wb, 2);
+                    uint8_t *sf = sm_sf + s * C::SF_BYTES;
+                    uint4 la;
+                    la.x = __shfl_sync(FULL, wa, 0);
+                    la.y = __shfl_sync(FULL, wa, 4);
+                    la.z = __shfl_sync(FULL, wa, 8);
+                    la.w = __shfl_sync(FULL, wa, 12);
+                    *reinterpret_cast<uint4 *>(sf + lane * 16) = la;
+#pragma unroll
+                    for (int q = 0; q < C::SFB_CHUNKS; ++q) {
+                        uint4 lb;
+                        lb.x = __shfl_sync(FULL, wb, 16 * q + 0);
+                        lb.y = __shfl_sync(FULL, wb, 16 * q + 4);
+                        lb.z = __shfl_sync(FULL, wb, 16 * q + 8);
+                        lb.w = __shfl_sync(FULL, wb, 16 * q + 12);
+                        *reinterpret_cast<uint4 *>(sf + 512 * (1 + q) + lane * 16) = lb;
+                    }
+                }
+                // the lines, and grouped A rows written by cp.async, become visible
+                // to the tensor core's async-proxy reads
+                if (!promote || GROUPED) fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&ctl->sfready[s]);
+                    trace_event(c, TR_SCALE_READY, it);
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) mbar_arrive(&ctl->vempty[v]);
+            __syncwarp();
+        }
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------ epilogue / promotion
         const int q = warp & 3;                       // tensor-memory lane quarter
         const int h = (warp - EPI_WARP0) >> 2;        // column half
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        uint32_t u = 0;
+        constexpr int NCH = C::EPI_COLS / 32;         // 32-column chunks per warp
+        uint32_t uses0 = 0, uses1 = 0, pk = 0;
+        uint32_t pu0 = 0, pu1 = 0;   // promotion uses of buffers 0 / 1 (pfull phases)
         for (int i = 0; i < my_tiles; ++i) {
             const int v = i & 1;
             bool ok = wait_bar(&ctl->vfull[v], static_cast<uint32_t>(i >> 1) & 1u, ctl, c);
@@ -618,65 +662,66 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             __nv_bfloat16 *crow = e.C + static_cast<int64_t>(row_ok ? row : 0) * c.N + tt.n0;
 
             if (!promote) {
-                const uint32_t buf = u & 1u;
-                ok = wait_bar(&ctl->tfull[buf], (u >> 1) & 1u, ctl, c);
-                ok = __all_sync(FULL, ok);
+                ok = __all_sync(FULL, wait_bar(&ctl->tfull[0], uses0 & 1u, ctl, c));
                 if (!ok) break;
-                if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_FULL_OK, static_cast<int>(u));
+                if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_FULL, i);
                 tc_fence_after();
-#pragma unroll 1
-                for (int ch = 0; ch < C::EPI_COLS / 32; ++ch) {
-                    uint32_t r[32];
-                    const int col = col0 + 32 * ch;
-                    tmem_ld_x32(tmem + lane_base + buf * BN + col, r);
-                    tmem_ld_wait();
-                    if (ch == C::EPI_COLS / 32 - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
-                        if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_RELEASED, static_cast<int>(u));
-                    }
-                    if (row_ok && tt.n0 + col < c.N) store_bf16x32(crow + col, r);
+                // drain the whole accumulator slice, then release it at once
+                uint32_t r[NCH][32];
+#pragma unroll
+                for (int x = 0; x < NCH; ++x) tmem_ld_x32(tmem + lane_base + col0 + 32 * x, r[x]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->tempty[0]);
+                if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_RELEASED, i);
+                ++uses0;
+                if (row_ok) {
+#pragma unroll
+                    for (int x = 0; x < NCH; ++x)
+                        if (tt.n0 + col0 + 32 * x < c.N) store_bf16x32(crow + col0 + 32 * x, r[x]);
                 }
-                ++u;
+                if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_STORED, i);
             } else {
-                constexpr int NCH = C::EPI_COLS / 32;
+                if (pk & 1u) ++pk;
                 float acc[C::EPI_COLS];
 #pragma unroll
                 for (int x = 0; x < C::EPI_COLS; ++x) acc[x] = 0.0f;
                 for (int kb = 0; kb < c.KB; ++kb) {
-                    const uint32_t buf = u & 1u;
-                    ok = wait_bar(&ctl->pfull[buf], (u >> 1) & 1u, ctl, c) &&
-                         wait_bar(&ctl->tfull[buf], (u >> 1) & 1u, ctl, c);
+                    const uint32_t b = pk & 1u;
+                    const uint32_t ub = b ? uses1 : uses0;
+                    const uint32_t pb = b ? pu1 : pu0;
+                    ok = wait_bar(&ctl->pfull[b], pb & 1u, ctl, c) &&
+                         wait_bar(&ctl->tfull[b], ub & 1u, ctl, c);
                     ok = __all_sync(FULL, ok);
                     if (!ok) break;
-                    if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_FULL_OK, static_cast<int>(u));
                     tc_fence_after();
                     float sc[NCH];
 #pragma unroll
-                    for (int x = 0; x < NCH; ++x) sc[x] = sm_ps[buf * C::PS_FLOATS + q * NBB + h * NCH + x];
-                    uint32_t r[NCH][32];
+                    for (int x = 0; x < NCH; ++x) sc[x] = sm_ps[b * C::PS_FLOATS + q * NBB + h * NCH + x];
+                    const uint32_t pbase = tmem + lane_base + b * BN + col0;
 #pragma unroll
-                    for (int x = 0; x < NCH; ++x) tmem_ld_x32(tmem + lane_base + buf * BN + col0 + 32 * x, r[x]);
-                    tmem_ld_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
-                    if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_RELEASED, static_cast<int>(u));
-                    ++u;
+                    for (int x = 0; x < 2 * NCH; ++x) {
+                        uint32_t r[16];
+                        tmem_ld_x16(pbase + 16 * x, r);
+                        tmem_ld_wait();
+                        if (x == 2 * NCH - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+                        }
 #pragma unroll
-                    for (int x = 0; x < NCH; ++x)
-#pragma unroll
-                        for (int y = 0; y < 32; ++y)
-                            acc[32 * x + y] = fmaf(sc[x], __uint_as_float(r[x][y]), acc[32 * x + y]);
+                        for (int y = 0; y < 16; ++y)
+                            acc[16 * x + y] = fmaf(sc[x >> 1], __uint_as_float(r[y]), acc[16 * x + y]);
+                    }
+                    if (b) { ++uses1; ++pu1; } else { ++uses0; ++pu0; }
+                    ++pk;
                 }
                 if (!ok) break;
                 if (row_ok) {
 #pragma unroll
-                    for (int x = 0; x < NCH; ++x) {
-                        const int col = col0 + 32 * x;
-                        if (tt.n0 + col < c.N) store_bf16x32f(crow + col, acc + 32 * x);
-                    }
+                    for (int x = 0; x < NCH; ++x)
+                        if (tt.n0 + col0 + 32 * x < c.N) store_bf16x32f(crow + col0 + 32 * x, acc + 32 * x);
                 }
             }
             __syncwarp();
