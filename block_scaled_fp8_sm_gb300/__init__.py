@@ -15,7 +15,7 @@ from ._abi import (FP8_PATH_AUTO, FP8_PATH_NATIVE, FP8_PATH_PROMOTE,  # noqa: F4
                    FP8_DEBUG_WAIT_LIMIT_CYCLES, FP8_DEBUG_WITHHOLD_STAGE, FP8_DEBUG_TRACE_BUFFER,
                    FP8_MAX_GROUPS_PER_LAUNCH, fp8_group_desc)
 
-__all__ = ["fp8_gemm_blockscaled", "fp8_gemm_grouped", "fp8_status_query", "fp8_strerror",
+__all__ = ["fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_gemm_grouped", "fp8_status_query", "fp8_strerror",
            "fp8_version", "fp8_debug_set", "fp8_lib_shutdown", "Fp8Error", "library"]
 
 
@@ -62,6 +62,21 @@ def fp8_gemm_blockscaled(A, sA, B, sB, C, M=None, N=None, K=None, stream=None, m
         rc = lib.fp8_gemm_blockscaled_ex(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C), M, N, K,
                                          int(mode), s)
     _check(rc, "fp8_gemm_blockscaled")
+    return C
+
+
+def fp8_gemm_blockscaled_noalloc(A, sA, B, sB, C, M=None, N=None, K=None, stream=None):
+    """Same as fp8_gemm_blockscaled (AUTO path) through the entry point that
+    allocates no device memory (its status word is a static array inside the
+    library).  For callers that cannot allocate device memory, e.g. a server
+    whose caching allocator owns the device.  Make the first call on a device
+    outside stream capture: it performs that device's one-time set-up."""
+    M = A.shape[0] if M is None else M
+    K = A.shape[1] if K is None else K
+    N = B.shape[0] if N is None else N
+    rc = library().fp8_gemm_blockscaled_noalloc(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C),
+                                                M, N, K, _stream(stream))
+    _check(rc, "fp8_gemm_blockscaled_noalloc")
     return C
 
 

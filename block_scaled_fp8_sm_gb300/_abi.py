@@ -35,7 +35,7 @@ FP8_MAX_GROUPS_PER_LAUNCH = 64
 EXPORTS = (
     "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_ex", "fp8_gemm_grouped",
     "fp8_gemm_grouped_ex", "fp8_status_query", "fp8_strerror", "fp8_version",
-    "fp8_debug_set", "fp8_lib_shutdown",
+    "fp8_debug_set", "fp8_lib_shutdown", "fp8_gemm_blockscaled_noalloc",
 )
 
 
@@ -61,6 +61,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fp8_gemm_blockscaled.restype = ci
     lib.fp8_gemm_blockscaled_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
     lib.fp8_gemm_blockscaled_ex.restype = ci
+    lib.fp8_gemm_blockscaled_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
+    lib.fp8_gemm_blockscaled_noalloc.restype = ci
     lib.fp8_gemm_grouped.argtypes = [ctypes.POINTER(fp8_group_desc), vp, i64, i64, i32, vp]
     lib.fp8_gemm_grouped.restype = ci
     lib.fp8_gemm_grouped_ex.argtypes = [ctypes.POINTER(fp8_group_desc), vp, i64, i64, i32, ci, vp]

@@ -215,6 +215,108 @@ int launch_grouped(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, i
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
+// ------------------------------------------- allocation-free entry point ----
+// fp8_gemm_blockscaled_noalloc runs the same kernel, but the device status
+// word it needs lives in this file-scope array instead of memory obtained from
+// cudaMalloc.  Every GPU that loads the library holds these 256 bytes until
+// the process exits.  Host code only ever uses the address returned by
+// cudaGetSymbolAddress for the current device: the name itself is a host-side
+// stand-in, not a device pointer.
+constexpr int kNoAllocScratchWords = 64;   // 256 bytes; word 0 is the status word
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
+
+struct NoAllocState {
+    bool ready = false;
+    int error = FP8_OK;
+    int sm_count = 0;
+    uint32_t *scratch = nullptr;   // device address of g_noalloc_scratch on this device
+};
+NoAllocState g_noalloc[MAX_DEVICES];
+
+// One-time set-up of the current device for the allocation-free entry point:
+// architecture check, kernel attributes, and the device address of the
+// static scratch array (cleared once).  Allocates nothing.
+int noalloc_setup(NoAllocState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8_ERR_CUDA;
+    if (dev < 0 || dev >= MAX_DEVICES) return FP8_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    NoAllocState &st = g_noalloc[dev];
+    if (st.ready) {
+        *out = &st;
+        return st.error;
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FP8_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+        st.ready = true;
+        st.error = FP8_ERR_ARCH;
+        *out = &st;
+        return FP8_ERR_ARCH;
+    }
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return FP8_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (set_kernel_attrs<TILE_N>() != FP8_OK) return FP8_ERR_CUDA;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return FP8_ERR_CUDA;
+    // the status word must start at zero; later calls only OR bits into it
+    if (cudaMemset(p, 0, sizeof(uint32_t) * kNoAllocScratchWords) != cudaSuccess)
+        return FP8_ERR_CUDA;
+    st.scratch = static_cast<uint32_t *>(p);
+    st.sm_count = sms;
+    st.ready = true;
+    st.error = FP8_OK;
+    (void)wait_limit_locked();
+    *out = &st;
+    return FP8_OK;
+}
+
+template <int BN>
+int launch_plain_noalloc(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                         int64_t M, int64_t N, int64_t K, NoAllocState *st, cudaStream_t stream) {
+    PlainArgs args;
+    std::memset(&args, 0, sizeof args);
+    Common &c = args.c;
+    c.M = static_cast<int>(M);
+    c.N = static_cast<int>(N);
+    c.K = static_cast<int>(K);
+    c.KB = static_cast<int>(K / 32);
+    c.KS = static_cast<int>((K + BK - 1) / BK);
+    c.mt = static_cast<int>((M + BM - 1) / BM);
+    c.nt = static_cast<int>((N + BN - 1) / BN);
+    c.num_tiles = c.mt * c.nt;
+    c.mode = FP8_PATH_AUTO;
+    c.status = st->scratch;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        c.wait_limit = wait_limit_locked();
+        c.withhold_stage = -1;
+        c.trace = nullptr;
+    }
+    int rc = encode_kmajor(&args.tmA, A, M, K, BM);
+    if (rc != FP8_OK) return rc;
+    rc = encode_kmajor(&args.tmB, B, N, K, BN);
+    if (rc != FP8_OK) return rc;
+    args.e.A = static_cast<const uint8_t *>(A);
+    args.e.sA = sA;
+    args.e.sB = sB;
+    args.e.C = static_cast<__nv_bfloat16 *>(C);
+    const int grid = c.num_tiles < st->sm_count ? c.num_tiles : st->sm_count;
+    bsfp8_gemm_plain<BN><<<grid, NUM_THREADS, smem_bytes<BN>(), stream>>>(args);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace bsfp8
 
@@ -247,6 +349,29 @@ int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const
 int fp8_gemm_blockscaled(const void *A, const float *sA, const void *B, const float *sB, void *C,
                          int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     return fp8_gemm_blockscaled_ex(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, stream);
+}
+
+int fp8_gemm_blockscaled_noalloc(const void *A, const float *sA, const void *B, const float *sB,
+                                 void *C, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != FP8_OK) return rc;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!C) return FP8_ERR_NULL;
+    if (!aligned(C, 16)) return FP8_ERR_ALIGN;
+    if (K > 0) {
+        if (!A || !B || !sA || !sB) return FP8_ERR_NULL;
+        if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 4) || !aligned(sB, 4))
+            return FP8_ERR_ALIGN;
+    }
+    // the scratch is the fixed 256-byte array above; its size does not grow
+    // with M, N or K, so the shape checks above are the only size limits
+    static_assert(sizeof(uint32_t) * kNoAllocScratchWords <= FP8_NOALLOC_SCRATCH_BYTES,
+                  "scratch larger than the documented maximum");
+    NoAllocState *st = nullptr;
+    rc = noalloc_setup(&st);
+    if (rc != FP8_OK) return rc;
+    if (K == 0) return zero_fill(C, M * N, stream);
+    return launch_plain_noalloc<TILE_N>(A, sA, B, sB, C, M, N, K, st, stream);
 }
 
 int fp8_gemm_grouped_ex(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, int64_t K,

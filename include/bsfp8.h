@@ -88,6 +88,27 @@ int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const
                             void *C, int64_t M, int64_t N, int64_t K, int mode,
                             cudaStream_t stream);
 
+/* Allocation-free variant of fp8_gemm_blockscaled (AUTO path, same layouts,
+ * constraints and results).  The pages have no counterpart: this entry point
+ * exists for callers that cannot allocate device memory: an inference server
+ * whose caching allocator owns the whole device (a stray cudaMalloc there can
+ * fail, fragment the pool or stall the device while it synchronises), or a
+ * deployment whose memory budget is fixed at start-up and must not grow per
+ * call.  The only extra device memory the kernel needs (its status
+ * word) lives in a static array inside the library: FP8_NOALLOC_SCRATCH_BYTES
+ * on every GPU that loads the library, held until the process exits.  Its
+ * size does not depend on M, N or K, so no problem size exceeds it.
+ * The call never invokes cudaMalloc, cudaFree or any allocating routine.
+ * The first call on each device performs a one-time set-up for that device
+ * (looks up the array's device address and clears it); make that first call
+ * before any stream capture.  All calls share the array: calls that overlap
+ * on the GPU race on it (only their status bits mix; results are not
+ * affected).  Device-side conditions of these calls (a wait that ran out) go
+ * to that array, not to the word fp8_status_query reads. */
+#define FP8_NOALLOC_SCRATCH_BYTES 256
+int fp8_gemm_blockscaled_noalloc(const void *A, const float *sA, const void *B, const float *sB,
+                                 void *C, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* One group of a grouped launch: device pointers with the layouts above,
  * sized by that group's M_g (sA_g has ceil(M_g/32) group-local row blocks). */
 typedef struct fp8_group_desc {
