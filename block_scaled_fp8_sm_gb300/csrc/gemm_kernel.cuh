@@ -126,7 +126,10 @@ enum : int {
     TR_EPI_STORED = 7,      // epilogue warp 4: tile `i` stored
     TR_VERDICT = 8,         // verdict warp: tile `i` published
     TR_MMA_TILE = 9,        // MMA lane 0: tile `i` accumulator free, starting
-    TR_EVENTS = 10
+    TR_PROD_TMA = 10,       // producer: stage `it` TMA issued
+    TR_PROD_SCALES = 11,    // producer: stage `it` scale copies issued
+    TR_PROD_DONE = 12,      // producer: stage `it` completion arrivals registered
+    TR_EVENTS = 13
 };
 
 __device__ __forceinline__ void trace_event(const Common &c, int ev, int idx) {
@@ -149,7 +152,8 @@ struct GroupedArgs {
 
 template <int STAGES>
 struct Ctrl {
-    uint64_t full[STAGES];      // producer -> scale warp (TMA bytes + cp.async arrivals)
+    uint64_t full[STAGES];      // producer -> MMA warp (TMA bytes; grouped: + A-row cp.async)
+    uint64_t scfull[STAGES];    // producer -> scale warp (cp.async of the stage's scales)
     uint64_t sfready[STAGES];   // scale warp -> MMA warp
     uint64_t empty[STAGES];     // MMA commit -> producer
     uint64_t tfull[2];          // MMA commit -> epilogue (accumulator / partial b)
@@ -178,13 +182,18 @@ constexpr int smem_bytes() {
 }
 
 // ---------------------------------------------------------------------------
+// Bounded wait.  The waiting threads are parked in hardware (try_wait with a
+// suspend hint) rather than polling: many warps spinning on barriers would
+// take the shared-memory issue path away from the producer and MMA warps.
+// The abort flag and the clock budget are looked at between suspensions.
+constexpr uint32_t kSuspendHintNs = 200000;   // 0.2 ms per suspension at most
 template <int STAGES>
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Ctrl<STAGES> *ctl,
                                          const Common &c) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
         if (*reinterpret_cast<volatile int *>(&ctl->abort)) return false;
         if (clock64() - t0 > c.wait_limit) {
             *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
@@ -214,7 +223,8 @@ __device__ __forceinline__ uint32_t ue8m0_of(float v) { return (__float_as_uint(
 template <int BN, bool GROUPED, typename Args>
 struct Sched {
     const Args &a;
-    const Common &c;
+    const Common c;          // a copy in registers: the kernel parameters sit behind
+                             // generic loads once the argument block's address is taken
     const int *tile_start;
     const int *mg;
 
@@ -248,8 +258,10 @@ struct Sched {
         return r;
     }
 
-    __device__ __forceinline__ const GroupEntry &entry(int g) const {
-        if constexpr (!GROUPED) return a.e;
+    GroupEntry e0;           // plain problems: the one entry, in registers
+
+    __device__ __forceinline__ GroupEntry entry(int g) const {
+        if constexpr (!GROUPED) return e0;
         else return a.e[g];
     }
 };
@@ -291,7 +303,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     constexpr int S = C::STAGES;
     constexpr int NBB = C::NBB;
     constexpr uint32_t FULL = 0xFFFFFFFFu;
-    const Common &c = args.c;
+    const Common c = args.c;   // register copy (see Sched)
 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -307,8 +319,11 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            // lane 0's expect_tx arrival + one cp.async-completion arrival per producer lane
-            mbar_init(&ctl->full[s], 1 + 32);
+            // full: lane 0's expect_tx arrival (+ one A-row cp.async arrival per
+            // producer lane for grouped problems); scfull: one scale cp.async
+            // arrival per producer lane
+            mbar_init(&ctl->full[s], GROUPED ? 1 + 32 : 1);
+            mbar_init(&ctl->scfull[s], 32);
             mbar_init(&ctl->sfready[s], 1);
             mbar_init(&ctl->empty[s], 1);
         }
@@ -363,7 +378,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             ? (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                   static_cast<int>(gridDim.x)
             : 0;
-    const Sched<BN, GROUPED, Args> sch{args, c, ctl->tile_start, ctl->mg};
+    GroupEntry e0{};
+    if constexpr (!GROUPED) e0 = args.e;
+    const Sched<BN, GROUPED, Args> sch{args, c, ctl->tile_start, ctl->mg, e0};
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -384,7 +401,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             const int ti = it / c.KS;
             const int ks = it % c.KS;
             const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + ti * static_cast<int>(gridDim.x));
-            const GroupEntry &e = sch.entry(tt.g);
+            const GroupEntry e = sch.entry(tt.g);
             const int k0 = ks * BK;
             if (lane == 0) {
                 if constexpr (!GROUPED) {
@@ -395,6 +412,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     mbar_arrive_expect_tx(&ctl->full[s], C::B_BYTES);
                     tma_load_2d(&args.tmB[tt.g], &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0);
                 }
+                trace_event(c, TR_PROD_TMA, it);
             }
             // scales of this stage: sc[rb*4 + j] = sA[m0/32 + rb][kb0 + j] (rb < 4),
             // sc[16 + cb*4 + j] = sB[n0/32 + cb][kb0 + j] (cb < BN/32); absent
@@ -416,6 +434,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     const float *src = in ? e.sB + static_cast<int64_t>(nb) * c.KB + kb : e.sB;
                     cp_async_4(sc + 64 + 4 * x, src, in ? 4u : 0u);
                 }
+                if (lane == 0) trace_event(c, TR_PROD_SCALES, it);
+                cp_async_mbar_arrive_noinc(&ctl->scfull[s]);
+                if (lane == 0) trace_event(c, TR_PROD_DONE, it);
             }
             if constexpr (GROUPED) {
                 // A rows of this group: 16-byte cp.async into the 128-byte swizzled
@@ -430,8 +451,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     const uint8_t *src = e.A + static_cast<int64_t>(tt.m0 + r) * c.K + (in ? kk : 0);
                     cp_async_16(dst0 + r * 128 + ((ch ^ (r & 7)) << 4), src, in ? 16u : 0u);
                 }
+                cp_async_mbar_arrive_noinc(&ctl->full[s]);
             }
-            cp_async_mbar_arrive_noinc(&ctl->full[s]);
         }
         // drain: every armed stage's last phase must complete before the CTA exits
         if (lane == 0) {
@@ -439,6 +460,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 const int s = d % S;
                 if (s == withheld) continue;
                 wait_bar_drain(&ctl->full[s], static_cast<uint32_t>(d / S) & 1u, c.wait_limit);
+                wait_bar_drain(&ctl->scfull[s], static_cast<uint32_t>(d / S) & 1u, c.wait_limit);
             }
         }
     } else if (warp == 1) {
@@ -465,7 +487,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     const uint32_t sfa_base = tmem + C::SF_COL0;
                     for (int ks = 0; ks < c.KS && ok; ++ks) {
                         const int s = (it + ks) % S;
-                        ok = wait_bar(&ctl->sfready[s], static_cast<uint32_t>((it + ks) / S) & 1u, ctl, c);
+                        const uint32_t ph = static_cast<uint32_t>((it + ks) / S) & 1u;
+                        ok = wait_bar(&ctl->full[s], ph, ctl, c) && wait_bar(&ctl->sfready[s], ph, ctl, c);
                         if (!ok) break;
                         trace_event(c, TR_MMA_READY, it + ks);
                         tc_fence_after();
@@ -500,7 +523,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 if (pk & 1u) ++pk;   // promotion tiles start on buffer 0 (see the header)
                 for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
                     const int s = it % S;
-                    ok = __all_sync(FULL, wait_bar(&ctl->sfready[s], static_cast<uint32_t>(it / S) & 1u, ctl, c));
+                    ok = __all_sync(FULL, wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c) &&
+                                              wait_bar(&ctl->sfready[s], static_cast<uint32_t>(it / S) & 1u, ctl, c));
                     if (!ok) break;
                     const float *sc = sm_sc + s * C::SC_FLOATS;
                     const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
@@ -553,7 +577,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             int verdict = 1;
             if (c.mode != PATH_PROMOTE) {
                 const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x));
-                const GroupEntry &e = sch.entry(tt.g);
+                const GroupEntry e = sch.entry(tt.g);
                 const int MB = (tt.Mg + 31) / 32;
                 const int mb0 = tt.m0 / 32, mb1 = min(mb0 + BM / 32, MB);
                 const int nb0 = tt.n0 / 32, nb1 = min(nb0 + BN / 32, c.N / 32);
@@ -595,7 +619,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             const bool promote = ctl->verdict[v] != 0;
             for (int ks = 0; ks < c.KS; ++ks, ++it) {
                 const int s = it % S;
-                ok = __all_sync(FULL, wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c));
+                ok = wait_bar(&ctl->scfull[s], static_cast<uint32_t>(it / S) & 1u, ctl, c);
+                if (GROUPED) ok = ok && wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c);
+                ok = __all_sync(FULL, ok);
                 if (!ok) break;
                 if (lane == 0) trace_event(c, TR_SCALE_FULL, it);
                 if (!promote) {
@@ -655,7 +681,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             if (!ok) break;
             const bool promote = ctl->verdict[v] != 0;
             const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x));
-            const GroupEntry &e = sch.entry(tt.g);
+            const GroupEntry e = sch.entry(tt.g);
             const int row = tt.m0 + 32 * q + lane;
             const bool row_ok = row < tt.Mg;
             const int col0 = h * C::EPI_COLS;

@@ -163,7 +163,7 @@ int fp8_version(void);
  *   that pipeline stage (counted from 0 over the CTA's whole K loop), so the
  *   waits behind it run out; the output is then incomplete.  -1 (default)
  *   disables it.  Used by the bounded-wait test.
- * FP8_DEBUG_TRACE_BUFFER: device address (0 = off) of a buffer of 10 x 1024
+ * FP8_DEBUG_TRACE_BUFFER: device address (0 = off) of a buffer of 13 x 1024
  *   uint64 words; CTA 0 of later launches writes the SM clock of its pipeline
  *   events there (event e, index i at word e*1024 + i).  A profiling aid; the
  *   event numbering is listed with the kernel.
