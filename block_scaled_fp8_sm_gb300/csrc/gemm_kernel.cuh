@@ -384,83 +384,64 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        const int total = my_tiles * c.KS;
+        // Per stage only: wait for the slot, register the bytes, issue the
+        // TMA; tile coordinates are decoded once per tile (a single warp runs
+        // dependent integer chains slowly, so the per-stage path stays short).
+        int it = 0, s = 0;
+        uint32_t ph = 0;
         int withheld = -1;   // slot never armed (test hook), excluded from the drain
-        int it = 0;
-        for (; it < total; ++it) {
-            const int s = it % S;
-            const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
-            bool ok = wait_bar(&ctl->empty[s], ph ^ 1u, ctl, c);
-            ok = __all_sync(FULL, ok);
-            if (!ok) break;
-            if ((c.withhold_stage == it) && blockIdx.x == 0) {
-                withheld = s;
-                continue;
-            }
-            if (lane == 0) trace_event(c, TR_PROD_ISSUE, it);
-            const int ti = it / c.KS;
-            const int ks = it % c.KS;
-            const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + ti * static_cast<int>(gridDim.x));
+        bool ok = true;
+        for (int i = 0; i < my_tiles && ok; ++i) {
+            const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x));
             const GroupEntry e = sch.entry(tt.g);
-            const int k0 = ks * BK;
-            if (lane == 0) {
-                if constexpr (!GROUPED) {
-                    mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
-                    tma_load_2d(&args.tmA, &ctl->full[s], sm_a + s * C::A_BYTES, k0, tt.m0);
-                    tma_load_2d(&args.tmB, &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0);
+            const CUtensorMap *tmb;
+            if constexpr (GROUPED) tmb = &args.tmB[tt.g];
+            else tmb = &args.tmB;
+            const int a_rows = min(BM, tt.Mg - tt.m0);   // grouped: A rows loaded by cp.async
+            const uint8_t *a_base = e.A + static_cast<int64_t>(tt.m0) * c.K;
+            for (int ks = 0, k0 = 0; ks < c.KS; ++ks, k0 += BK) {
+                ok = __all_sync(FULL, wait_bar(&ctl->empty[s], ph ^ 1u, ctl, c));
+                if (!ok) break;
+                if ((c.withhold_stage == it) && blockIdx.x == 0) {
+                    withheld = s;
                 } else {
-                    mbar_arrive_expect_tx(&ctl->full[s], C::B_BYTES);
-                    tma_load_2d(&args.tmB[tt.g], &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0);
+                    if (lane == 0) {
+                        trace_event(c, TR_PROD_ISSUE, it);
+                        if constexpr (!GROUPED) {
+                            mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
+                            tma_load_2d(&args.tmA, &ctl->full[s], sm_a + s * C::A_BYTES, k0, tt.m0);
+                        } else {
+                            mbar_arrive_expect_tx(&ctl->full[s], C::B_BYTES);
+                        }
+                        tma_load_2d(tmb, &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0);
+                        trace_event(c, TR_PROD_TMA, it);
+                    }
+                    if constexpr (GROUPED) {
+                        // A rows of this group: 16-byte cp.async into the 128-byte
+                        // swizzled layout; chunks past K are zero-filled, rows past
+                        // M_g are not loaded (they only feed output rows that are
+                        // never stored).
+                        const uint32_t dst0 = smem_u32(sm_a + s * C::A_BYTES);
+                        for (int idx = lane; idx < a_rows * 8; idx += 32) {
+                            const int r = idx >> 3, ch = idx & 7;
+                            const int kk = k0 + ch * 16;
+                            const bool in = kk < c.K;
+                            cp_async_16(dst0 + r * 128 + ((ch ^ (r & 7)) << 4),
+                                        a_base + static_cast<int64_t>(r) * c.K + (in ? kk : 0), in ? 16u : 0u);
+                        }
+                        cp_async_mbar_arrive_noinc(&ctl->full[s]);
+                    }
                 }
-                trace_event(c, TR_PROD_TMA, it);
-            }
-            // scales of this stage: sc[rb*4 + j] = sA[m0/32 + rb][kb0 + j] (rb < 4),
-            // sc[16 + cb*4 + j] = sB[n0/32 + cb][kb0 + j] (cb < BN/32); absent
-            // blocks are zero-filled (they only meet discarded rows or K past the end)
-            {
-                const uint32_t sc = smem_u32(sm_sc + s * C::SC_FLOATS);
-                const int kb = ks * KB_PER_STAGE + (lane & 3);
-                const bool kb_ok = kb < c.KB;
-                if (lane < 16) {
-                    const int mb = tt.m0 / 32 + (lane >> 2);
-                    const bool in = kb_ok && mb < (tt.Mg + 31) / 32;
-                    const float *src = in ? e.sA + static_cast<int64_t>(mb) * c.KB + kb : e.sA;
-                    cp_async_4(sc + 4 * lane, src, in ? 4u : 0u);
-                }
-#pragma unroll
-                for (int x = lane; x < 4 * NBB; x += 32) {
-                    const int nb = tt.n0 / 32 + (x >> 2);
-                    const bool in = kb_ok && nb < c.N / 32;
-                    const float *src = in ? e.sB + static_cast<int64_t>(nb) * c.KB + kb : e.sB;
-                    cp_async_4(sc + 64 + 4 * x, src, in ? 4u : 0u);
-                }
-                if (lane == 0) trace_event(c, TR_PROD_SCALES, it);
-                cp_async_mbar_arrive_noinc(&ctl->scfull[s]);
-                if (lane == 0) trace_event(c, TR_PROD_DONE, it);
-            }
-            if constexpr (GROUPED) {
-                // A rows of this group: 16-byte cp.async into the 128-byte swizzled
-                // layout; chunks past K are zero-filled, rows past M_g are not
-                // loaded (they only feed output rows that are never stored).
-                const int rows = min(BM, tt.Mg - tt.m0);
-                const uint32_t dst0 = smem_u32(sm_a + s * C::A_BYTES);
-                for (int idx = lane; idx < rows * 8; idx += 32) {
-                    const int r = idx >> 3, ch = idx & 7;
-                    const int kk = k0 + ch * 16;
-                    const bool in = kk < c.K;
-                    const uint8_t *src = e.A + static_cast<int64_t>(tt.m0 + r) * c.K + (in ? kk : 0);
-                    cp_async_16(dst0 + r * 128 + ((ch ^ (r & 7)) << 4), src, in ? 16u : 0u);
-                }
-                cp_async_mbar_arrive_noinc(&ctl->full[s]);
+                ++it;
+                if (++s == S) { s = 0; ph ^= 1u; }
             }
         }
         // drain: every armed stage's last phase must complete before the CTA exits
         if (lane == 0) {
             for (int d = max(0, it - S); d < it; ++d) {
-                const int s = d % S;
-                if (s == withheld) continue;
-                wait_bar_drain(&ctl->full[s], static_cast<uint32_t>(d / S) & 1u, c.wait_limit);
-                wait_bar_drain(&ctl->scfull[s], static_cast<uint32_t>(d / S) & 1u, c.wait_limit);
+                const int sd = d % S;
+                if (sd == withheld) continue;
+                wait_bar_drain(&ctl->full[sd], static_cast<uint32_t>(d / S) & 1u, c.wait_limit);
             }
         }
     } else if (warp == 1) {
@@ -610,24 +591,67 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         }
     } else if (warp == 3) {
         // --------------------------------------------------------- scale warp
-        int it = 0;
+        // Loads each stage's fp32 block scales with cp.async (lane l < 16:
+        // sA[m0/32 + l/4][kb0 + l%4]; lane l < 4*BN/32: sB[n0/32 + l/4][kb0 +
+        // l%4]) L stages ahead of turning them into the UE8M0 lines that
+        // tcgen05.cp replicates into all lane quarters.  Absent blocks read as
+        // zero: they only meet discarded rows or K past the end.
+        constexpr int L = 2;
+        const int total = my_tiles * c.KS;
+        // issue side (stage it)
+        int ii = -1, iks = c.KS;            // tile / stage-in-tile of the next issue
+        int is = 0;
+        uint32_t iph = 0;
+        const float *pa = nullptr, *pb = nullptr;
+        bool a_in = false, b_in = false;
+        // build side (stage it - L)
+        int bi = -1, bks = c.KS, bs = 0;
+        uint32_t bph = 0;
+        bool promote = false;
         bool ok = true;
-        for (int i = 0; i < my_tiles && ok; ++i) {
-            const int v = i & 1;
-            ok = __all_sync(FULL, wait_bar(&ctl->vfull[v], static_cast<uint32_t>(i >> 1) & 1u, ctl, c));
-            if (!ok) break;
-            const bool promote = ctl->verdict[v] != 0;
-            for (int ks = 0; ks < c.KS; ++ks, ++it) {
-                const int s = it % S;
-                ok = wait_bar(&ctl->scfull[s], static_cast<uint32_t>(it / S) & 1u, ctl, c);
-                if (GROUPED) ok = ok && wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c);
-                ok = __all_sync(FULL, ok);
+        for (int it = 0; it < total + L && ok; ++it) {
+            if (it < total) {
+                if (++iks >= c.KS) {   // next tile: per-lane source pointers
+                    iks = 0;
+                    ++ii;
+                    const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + ii * static_cast<int>(gridDim.x));
+                    const GroupEntry e = sch.entry(tt.g);
+                    const int mb = tt.m0 / 32 + (lane >> 2);
+                    const int nb = tt.n0 / 32 + (lane >> 2);
+                    a_in = lane < 16 && mb < (tt.Mg + 31) / 32;
+                    b_in = lane < 4 * NBB && nb < c.N / 32;
+                    pa = e.sA + (a_in ? static_cast<int64_t>(mb) * c.KB + (lane & 3) : 0);
+                    pb = e.sB + (b_in ? static_cast<int64_t>(nb) * c.KB + (lane & 3) : 0);
+                }
+                ok = __all_sync(FULL, wait_bar(&ctl->empty[is], iph ^ 1u, ctl, c));
                 if (!ok) break;
-                if (lane == 0) trace_event(c, TR_SCALE_FULL, it);
+                const uint32_t sc = smem_u32(sm_sc + is * C::SC_FLOATS);
+                const bool kb_ok = iks * KB_PER_STAGE + (lane & 3) < c.KB;
+                if (lane < 16) cp_async_4(sc + 4 * lane, pa, (a_in && kb_ok) ? 4u : 0u);
+                if (lane < 4 * NBB) cp_async_4(sc + 64 + 4 * lane, pb, (b_in && kb_ok) ? 4u : 0u);
+                cp_async_mbar_arrive_noinc(&ctl->scfull[is]);
+                if (a_in && kb_ok) pa += KB_PER_STAGE;
+                if (b_in && kb_ok) pb += KB_PER_STAGE;
+                if (++is == S) { is = 0; iph ^= 1u; }
+            }
+            if (it >= L) {
+                if (++bks >= c.KS) {   // next tile: its path
+                    bks = 0;
+                    ++bi;
+                    const int v = bi & 1;
+                    ok = __all_sync(FULL, wait_bar(&ctl->vfull[v], static_cast<uint32_t>(bi >> 1) & 1u, ctl, c));
+                    if (!ok) break;
+                    promote = ctl->verdict[v] != 0;
+                }
+                bool w = wait_bar(&ctl->scfull[bs], bph, ctl, c);
+                if (GROUPED) w = w && wait_bar(&ctl->full[bs], bph, ctl, c);
+                ok = __all_sync(FULL, w);
+                if (!ok) break;
+                if (lane == 0) trace_event(c, TR_SCALE_FULL, it - L);
                 if (!promote) {
-                    // UE8M0 lines for tcgen05.cp: 32 identical 16-byte lines per 128
-                    // rows; word w of a line = row block w, byte j = K block j.
-                    const float *sc = sm_sc + s * C::SC_FLOATS;
+                    // 32 identical 16-byte lines per 128 rows; word w of a line =
+                    // row block w, byte j = K block j of the stage.
+                    const float *sc = sm_sc + bs * C::SC_FLOATS;
                     const float va = lane < 16 ? sc[lane] : 1.0f;
                     const float vb = lane < 4 * NBB ? sc[16 + lane] : 1.0f;
                     uint32_t wa = ue8m0_of(va) << (8 * (lane & 3));
@@ -636,7 +660,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     uint32_t wb = ue8m0_of(vb) << (8 * (lane & 3));
                     wb |= __shfl_xor_sync(FULL, wb, 1);
                     wb |= __shfl_xor_sync(FULL, wb, 2);
-                    uint8_t *sf = sm_sf + s * C::SF_BYTES;
+                    uint8_t *sf = sm_sf + bs * C::SF_BYTES;
                     uint4 la;
                     la.x = __shfl_sync(FULL, wa, 0);
                     la.y = __shfl_sync(FULL, wa, 4);
@@ -658,14 +682,16 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 if (!promote || GROUPED) fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&ctl->sfready[s]);
-                    trace_event(c, TR_SCALE_READY, it);
+                    mbar_arrive(&ctl->sfready[bs]);
+                    trace_event(c, TR_SCALE_READY, it - L);
+                    if (bks == c.KS - 1) mbar_arrive(&ctl->vempty[bi & 1]);
                 }
+                __syncwarp();
+                if (++bs == S) { bs = 0; bph ^= 1u; }
             }
-            if (!ok) break;
-            if (lane == 0) mbar_arrive(&ctl->vempty[v]);
-            __syncwarp();
         }
+        // no scale copy may still be landing when the CTA exits
+        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------ epilogue / promotion
         const int q = warp & 3;                       // tensor-memory lane quarter
