@@ -82,13 +82,14 @@ struct Cfg {
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;           // 128 B rows per tcgen05.cp
     static constexpr int SF_BYTES = 512 * (1 + SFB_CHUNKS);         // scale lines per stage
     static constexpr int SF_COLS = 4 * (1 + SFB_CHUNKS);            // tensor-memory columns per stage
-    static constexpr int SF_COL0 = (2 * BN + STAGES * SF_COLS <= 512) ? 2 * BN : BN;
+    static constexpr int SF_STAGES = 8;                             // scale ring depth (runs ahead of the operand ring)
+    static constexpr int SF_COL0 = (2 * BN + SF_STAGES * SF_COLS <= 512) ? 2 * BN : BN;
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_COLS = BN / 2;                         // columns per epilogue warp
     static constexpr int NBB = BN / 32;                             // 32-column blocks per tile
     static constexpr int SC_FLOATS = 16 + 4 * NBB;                  // staged fp32 scales per stage
     static constexpr int PS_FLOATS = 4 * NBB;                       // scale products per K block
-    static_assert(SF_COL0 + STAGES * SF_COLS <= 512 && SF_COL0 >= BN, "tensor memory budget");
+    static_assert(SF_COL0 + SF_STAGES * SF_COLS <= 512 && SF_COL0 >= BN, "tensor memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
     static_assert(4 * NBB <= 32, "one scale product per MMA-warp lane");
 };
@@ -150,12 +151,13 @@ struct GroupedArgs {
     Common c;
 };
 
-template <int STAGES>
+template <int STAGES, int SF_STAGES>
 struct Ctrl {
-    uint64_t full[STAGES];      // producer -> MMA warp (TMA bytes; grouped: + A-row cp.async)
-    uint64_t scfull[STAGES];    // producer -> scale warp (cp.async of the stage's scales)
-    uint64_t sfready[STAGES];   // scale warp -> MMA warp
-    uint64_t empty[STAGES];     // MMA commit -> producer
+    uint64_t full[STAGES];        // producer -> MMA warp (TMA bytes; grouped: + A-row cp.async)
+    uint64_t empty[STAGES];       // MMA commit -> producer
+    uint64_t scfull[SF_STAGES];   // scale cp.async landed -> scale warp
+    uint64_t sfready[SF_STAGES];  // scale warp -> MMA warp (lines written)
+    uint64_t sfempty[SF_STAGES];  // MMA commit -> scale warp (lines and scales consumed)
     uint64_t tfull[2];          // MMA commit -> epilogue (accumulator / partial b)
     uint64_t tempty[2];         // epilogue -> MMA
     uint64_t pfull[2];          // MMA warp -> epilogue (scale products of partial b)
@@ -177,8 +179,9 @@ struct Tile {
 template <int BN>
 constexpr int smem_bytes() {
     using C = Cfg<BN>;
-    return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES + C::SF_BYTES + 4 * C::SC_FLOATS) +
-           2 * 4 * C::PS_FLOATS + static_cast<int>(sizeof(Ctrl<C::STAGES>));
+    return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES) +
+           C::SF_STAGES * (C::SF_BYTES + 4 * C::SC_FLOATS) + 2 * 4 * C::PS_FLOATS +
+           static_cast<int>(sizeof(Ctrl<C::STAGES, C::SF_STAGES>));
 }
 
 // ---------------------------------------------------------------------------
@@ -187,8 +190,8 @@ constexpr int smem_bytes() {
 // take the shared-memory issue path away from the producer and MMA warps.
 // The abort flag and the clock budget are looked at between suspensions.
 constexpr uint32_t kSuspendHintNs = 200000;   // 0.2 ms per suspension at most
-template <int STAGES>
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Ctrl<STAGES> *ctl,
+template <typename CtrlT>
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, CtrlT *ctl,
                                          const Common &c) {
     if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
     const long long t0 = clock64();
@@ -199,6 +202,27 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Ctrl<ST
             *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
             atomicOr(c.status, STATUS_TIMEOUT);
             return false;
+        }
+    }
+}
+
+// Latency-critical wait of the single MMA-issuing thread: polls without
+// suspending (a woken thread resumes a few hundred cycles late) and looks at
+// the clock / abort flag every 256 polls.
+template <typename CtrlT>
+__device__ __forceinline__ bool wait_spin(uint64_t *bar, uint32_t parity, CtrlT *ctl,
+                                          const Common &c) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((n & 255u) == 0u) {
+            if (*reinterpret_cast<volatile int *>(&ctl->abort)) return false;
+            if (clock64() - t0 > c.wait_limit) {
+                *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
+                atomicOr(c.status, STATUS_TIMEOUT);
+                return false;
+            }
         }
     }
 }
@@ -309,10 +333,12 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sm_a = smem;
     uint8_t *sm_b = sm_a + S * C::A_BYTES;
-    uint8_t *sm_sf = sm_b + S * C::B_BYTES;
-    float *sm_sc = reinterpret_cast<float *>(sm_sf + S * C::SF_BYTES);       // [S][SC_FLOATS]
-    float *sm_ps = sm_sc + S * C::SC_FLOATS;                                   // [2][PS_FLOATS]
-    Ctrl<S> *ctl = reinterpret_cast<Ctrl<S> *>(sm_ps + 2 * C::PS_FLOATS);
+    uint8_t *sm_sf = sm_b + S * C::B_BYTES;                                  // [FS][SF_BYTES]
+    constexpr int FS = C::SF_STAGES;
+    float *sm_sc = reinterpret_cast<float *>(sm_sf + FS * C::SF_BYTES);      // [FS][SC_FLOATS]
+    float *sm_ps = sm_sc + FS * C::SC_FLOATS;                                  // [2][PS_FLOATS]
+    using CtrlT = Ctrl<S, FS>;
+    CtrlT *ctl = reinterpret_cast<CtrlT *>(sm_ps + 2 * C::PS_FLOATS);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -323,9 +349,12 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             // producer lane for grouped problems); scfull: one scale cp.async
             // arrival per producer lane
             mbar_init(&ctl->full[s], GROUPED ? 1 + 32 : 1);
-            mbar_init(&ctl->scfull[s], 32);
-            mbar_init(&ctl->sfready[s], 1);
             mbar_init(&ctl->empty[s], 1);
+        }
+        for (int f = 0; f < FS; ++f) {
+            mbar_init(&ctl->scfull[f], 32);   // one cp.async arrival per scale-warp lane
+            mbar_init(&ctl->sfready[f], 1);
+            mbar_init(&ctl->sfempty[f], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tfull[b], 1);
@@ -469,13 +498,16 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     for (int ks = 0; ks < c.KS && ok; ++ks) {
                         const int s = (it + ks) % S;
                         const uint32_t ph = static_cast<uint32_t>((it + ks) / S) & 1u;
-                        ok = wait_bar(&ctl->full[s], ph, ctl, c) && wait_bar(&ctl->sfready[s], ph, ctl, c);
+                        const int f = (it + ks) % FS;
+                        const uint32_t phf = static_cast<uint32_t>((it + ks) / FS) & 1u;
+                        ok = wait_spin(&ctl->sfready[f], phf, ctl, c) && wait_spin(&ctl->full[s], ph, ctl, c);
                         if (!ok) break;
                         trace_event(c, TR_MMA_READY, it + ks);
+                        if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
                         tc_fence_after();
-                        const uint32_t sfa = sfa_base + s * C::SF_COLS;
+                        const uint32_t sfa = sfa_base + f * C::SF_COLS;
                         const uint32_t sfb = sfa + 4;
-                        const uint32_t sf_s = smem_u32(sm_sf + s * C::SF_BYTES);
+                        const uint32_t sf_s = smem_u32(sm_sf + f * C::SF_BYTES);
                         tmem_cp_32x128b_warpx4(sfa, sdesc_sf_lines(sf_s));
 #pragma unroll
                         for (int q = 0; q < C::SFB_CHUNKS; ++q)
@@ -490,6 +522,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                                          idesc_mxf8f6f4(BM, BN, j, j), sfa, sfb, (ks | j) != 0 ? 1u : 0u);
                         }
                         mma_commit(&ctl->empty[s]);
+                        mma_commit(&ctl->sfempty[f]);
                         trace_event(c, TR_MMA_ISSUED, it + ks);
                         issued = true;
                     }
@@ -504,10 +537,12 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 if (pk & 1u) ++pk;   // promotion tiles start on buffer 0 (see the header)
                 for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
                     const int s = it % S;
+                    const int f = it % FS;
                     ok = __all_sync(FULL, wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c) &&
-                                              wait_bar(&ctl->sfready[s], static_cast<uint32_t>(it / S) & 1u, ctl, c));
+                                              wait_bar(&ctl->sfready[f], static_cast<uint32_t>(it / FS) & 1u, ctl, c));
                     if (!ok) break;
-                    const float *sc = sm_sc + s * C::SC_FLOATS;
+                    if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
+                    const float *sc = sm_sc + f * C::SC_FLOATS;
                     const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
                     const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
                     const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
@@ -534,7 +569,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         ++pk;
                     }
                     if (!ok) break;
-                    if (lane == 0) mma_commit(&ctl->empty[s]);
+                    if (lane == 0) {
+                        mma_commit(&ctl->empty[s]);
+                        mma_commit(&ctl->sfempty[f]);
+                    }
                     __syncwarp();
                 }
                 if (!ok) break;
@@ -596,7 +634,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         // l%4]) L stages ahead of turning them into the UE8M0 lines that
         // tcgen05.cp replicates into all lane quarters.  Absent blocks read as
         // zero: they only meet discarded rows or K past the end.
-        constexpr int L = 2;
+        constexpr int L = 4;
         const int total = my_tiles * c.KS;
         // issue side (stage it)
         int ii = -1, iks = c.KS;            // tile / stage-in-tile of the next issue
@@ -623,7 +661,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     pa = e.sA + (a_in ? static_cast<int64_t>(mb) * c.KB + (lane & 3) : 0);
                     pb = e.sB + (b_in ? static_cast<int64_t>(nb) * c.KB + (lane & 3) : 0);
                 }
-                ok = __all_sync(FULL, wait_bar(&ctl->empty[is], iph ^ 1u, ctl, c));
+                ok = __all_sync(FULL, wait_bar(&ctl->sfempty[is], iph ^ 1u, ctl, c));
                 if (!ok) break;
                 const uint32_t sc = smem_u32(sm_sc + is * C::SC_FLOATS);
                 const bool kb_ok = iks * KB_PER_STAGE + (lane & 3) < c.KB;
@@ -632,7 +670,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 cp_async_mbar_arrive_noinc(&ctl->scfull[is]);
                 if (a_in && kb_ok) pa += KB_PER_STAGE;
                 if (b_in && kb_ok) pb += KB_PER_STAGE;
-                if (++is == S) { is = 0; iph ^= 1u; }
+                if (++is == FS) { is = 0; iph ^= 1u; }
             }
             if (it >= L) {
                 if (++bks >= c.KS) {   // next tile: its path
@@ -643,9 +681,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     if (!ok) break;
                     promote = ctl->verdict[v] != 0;
                 }
-                bool w = wait_bar(&ctl->scfull[bs], bph, ctl, c);
-                if (GROUPED) w = w && wait_bar(&ctl->full[bs], bph, ctl, c);
-                ok = __all_sync(FULL, w);
+                ok = __all_sync(FULL, wait_bar(&ctl->scfull[bs], bph, ctl, c));
                 if (!ok) break;
                 if (lane == 0) trace_event(c, TR_SCALE_FULL, it - L);
                 if (!promote) {
@@ -677,9 +713,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         *reinterpret_cast<uint4 *>(sf + 512 * (1 + q) + lane * 16) = lb;
                     }
                 }
-                // the lines, and grouped A rows written by cp.async, become visible
-                // to the tensor core's async-proxy reads
-                if (!promote || GROUPED) fence_proxy_async_smem();
+                // the lines become visible to tcgen05.cp's async-proxy reads
+                if (!promote) fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&ctl->sfready[bs]);
@@ -687,7 +722,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     if (bks == c.KS - 1) mbar_arrive(&ctl->vempty[bi & 1]);
                 }
                 __syncwarp();
-                if (++bs == S) { bs = 0; bph ^= 1u; }
+                if (++bs == FS) { bs = 0; bph ^= 1u; }
             }
         }
         // no scale copy may still be landing when the CTA exits
