@@ -57,6 +57,9 @@ int set_kernel_attrs() {
     if (cudaFuncSetAttribute(bsfp8_gemm_grouped<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN>()) != cudaSuccess)
         return FP8_ERR_CUDA;
+    if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<BN, true>()) != cudaSuccess)
+        return FP8_ERR_CUDA;
     return FP8_OK;
 }
 
@@ -185,6 +188,29 @@ int launch_plain(const void *A, const float *sA, const void *B, const float *sB,
     args.e.C = static_cast<__nv_bfloat16 *>(C);
     int grid = args.c.num_tiles < d->sm_count ? args.c.num_tiles : d->sm_count;
     bsfp8_gemm_plain<BN><<<grid, NUM_THREADS, smem_bytes<BN>(), stream>>>(args);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+// CTA-pair launch: 256-row tiles, each CTA of a pair loads 128 rows of A and
+// 128 of B's 256 columns; the grid is a whole number of pairs.
+template <int BN>
+int launch_pair(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                int64_t M, int64_t N, int64_t K, int mode, DeviceState *d, cudaStream_t stream) {
+    PlainArgs args;
+    std::memset(&args, 0, sizeof args);
+    fill_common(args.c, M, N, K, mode, d, BN);
+    args.c.mt = static_cast<int>((M + 2 * BM - 1) / (2 * BM));
+    args.c.num_tiles = args.c.mt * args.c.nt;
+    int rc = encode_kmajor(&args.tmA, A, M, K, BM);
+    if (rc != FP8_OK) return rc;
+    rc = encode_kmajor(&args.tmB, B, N, K, BN / 2);
+    if (rc != FP8_OK) return rc;
+    args.e.A = static_cast<const uint8_t *>(A);
+    args.e.sA = sA;
+    args.e.sB = sB;
+    args.e.C = static_cast<__nv_bfloat16 *>(C);
+    const int pairs = args.c.num_tiles < d->sm_count / 2 ? args.c.num_tiles : d->sm_count / 2;
+    bsfp8_gemm_pair<BN><<<2 * pairs, NUM_THREADS, smem_bytes<BN, true>(), stream>>>(args);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -343,7 +369,7 @@ int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const
     rc = device_setup(&d);
     if (rc != FP8_OK) return rc;
     if (K == 0) return zero_fill(C, M * N, stream);
-    return launch_plain<TILE_N>(A, sA, B, sB, C, M, N, K, mode, d, stream);
+    return launch_pair<TILE_N>(A, sA, B, sB, C, M, N, K, mode, d, stream);
 }
 
 int fp8_gemm_blockscaled(const void *A, const float *sA, const void *B, const float *sB, void *C,

@@ -73,12 +73,14 @@ constexpr int TILE_N = 256;        // the BN every launch uses
 enum : uint32_t { STATUS_TIMEOUT = 1u, STATUS_SCALE = 2u };
 enum : int { PATH_AUTO = 0, PATH_NATIVE = 1, PATH_PROMOTE = 2 };
 
-template <int BN_>
+template <int BN_, bool PAIR_ = false>
 struct Cfg {
     static constexpr int BN = BN_;
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
-    static constexpr int A_BYTES = BM * BK;
-    static constexpr int B_BYTES = BN * BK;
+    static constexpr bool PAIR = PAIR_;   // CTA pair (cta_group::2): 256-row tiles, B split by columns
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;               // output rows per tile
+    static constexpr int STAGES = PAIR ? 6 : ((BN == 256) ? 4 : 6);
+    static constexpr int A_BYTES = BM * BK;                         // this CTA's A rows per stage
+    static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK;       // this CTA's B rows per stage
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;           // 128 B rows per tcgen05.cp
     static constexpr int SF_BYTES = 512 * (1 + SFB_CHUNKS);         // scale lines per stage
     static constexpr int SF_COLS = 4 * (1 + SFB_CHUNKS);            // tensor-memory columns per stage
@@ -176,9 +178,9 @@ struct Tile {
     int m0, n0, Mg, g;
 };
 
-template <int BN>
+template <int BN, bool PAIR = false>
 constexpr int smem_bytes() {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, PAIR>;
     return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES) +
            C::SF_STAGES * (C::SF_BYTES + 4 * C::SC_FLOATS) + 2 * 4 * C::PS_FLOATS +
            static_cast<int>(sizeof(Ctrl<C::STAGES, C::SF_STAGES>));
@@ -244,7 +246,7 @@ __device__ __forceinline__ bool is_pow2_scale(float v) {
 
 __device__ __forceinline__ uint32_t ue8m0_of(float v) { return (__float_as_uint(v) >> 23) & 0xFFu; }
 
-template <int BN, bool GROUPED, typename Args>
+template <int BN, bool GROUPED, typename Args, int TILE_M = BM>
 struct Sched {
     const Args &a;
     const Common c;          // a copy in registers: the kernel parameters sit behind
@@ -260,7 +262,7 @@ struct Sched {
             const int first_m = grp * GROUP_M;
             const int gsz = min(c.mt - first_m, GROUP_M);
             const int in = t - grp * per_group;
-            r.m0 = (first_m + in % gsz) * BM;
+            r.m0 = (first_m + in % gsz) * TILE_M;
             r.n0 = (in / gsz) * BN;
             r.Mg = c.M;
             r.g = 0;
@@ -321,9 +323,10 @@ __device__ __forceinline__ void store_bf16x32f(__nv_bfloat16 *dst, const float *
 }
 
 // ---------------------------------------------------------------------------
-template <int BN, bool GROUPED, typename Args>
+template <int BN, bool GROUPED, bool PAIR, typename Args>
 __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, PAIR>;
+    static_assert(!(PAIR && GROUPED), "CTA pairs are used for single problems only");
     constexpr int S = C::STAGES;
     constexpr int NBB = C::NBB;
     constexpr uint32_t FULL = 0xFFFFFFFFu;
@@ -342,6 +345,13 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // CTA pairs: rank 0 (the leader) issues the pair's MMAs; each CTA owns
+    // rows [rank*128, rank*128 + 128) of the tile and half of B's columns.
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0u;
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int row_off = static_cast<int>(rank) * BM;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -353,12 +363,12 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         }
         for (int f = 0; f < FS; ++f) {
             mbar_init(&ctl->scfull[f], 32);   // one cp.async arrival per scale-warp lane
-            mbar_init(&ctl->sfready[f], 1);
+            mbar_init(&ctl->sfready[f], (PAIR && leader) ? 2 : 1);   // the leader also waits for the peer's lines
             mbar_init(&ctl->sfempty[f], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tfull[b], 1);
-            mbar_init(&ctl->tempty[b], NUM_EPI_WARPS);
+            mbar_init(&ctl->tempty[b], (PAIR && leader) ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
             mbar_init(&ctl->pfull[b], 1);
             mbar_init(&ctl->vfull[b], 1);
             mbar_init(&ctl->vempty[b], 2 + NUM_EPI_WARPS);   // MMA + scale warp + epilogue
@@ -368,8 +378,13 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&ctl->tmem_base, C::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(&ctl->tmem_base, C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&ctl->tmem_base, C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     if (warp == 2) {
         if constexpr (GROUPED) {
@@ -398,18 +413,16 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // the peer's barriers exist before any remote arrive
     tc_fence_after();
 
     const uint32_t tmem = ctl->tmem_base;
     const int num_tiles = ctl->num_tiles;
-    const int my_tiles =
-        (static_cast<int>(blockIdx.x) < num_tiles)
-            ? (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                  static_cast<int>(gridDim.x)
-            : 0;
+    const int my_tiles = (unit < num_tiles) ? (num_tiles - unit + nunits - 1) / nunits : 0;
     GroupEntry e0{};
     if constexpr (!GROUPED) e0 = args.e;
-    const Sched<BN, GROUPED, Args> sch{args, c, ctl->tile_start, ctl->mg, e0};
+    const Sched<BN, GROUPED, Args, C::TILE_M> sch{args, c, ctl->tile_start, ctl->mg, e0};
+    constexpr uint16_t PAIR_MASK = 0x3;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -421,7 +434,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         int withheld = -1;   // slot never armed (test hook), excluded from the drain
         bool ok = true;
         for (int i = 0; i < my_tiles && ok; ++i) {
-            const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x));
+            const Tile tt = sch.tile(unit + i * nunits);
             const GroupEntry e = sch.entry(tt.g);
             const CUtensorMap *tmb;
             if constexpr (GROUPED) tmb = &args.tmB[tt.g];
@@ -436,13 +449,21 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 } else {
                     if (lane == 0) {
                         trace_event(c, TR_PROD_ISSUE, it);
-                        if constexpr (!GROUPED) {
-                            mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
-                            tma_load_2d(&args.tmA, &ctl->full[s], sm_a + s * C::A_BYTES, k0, tt.m0);
+                        if constexpr (PAIR) {
+                            // both CTAs' bytes complete on the leader's barrier
+                            const uint32_t bar_c = mapa_shared(&ctl->full[s], 0);
+                            if (leader) mbar_arrive_expect_tx(&ctl->full[s], 2 * (C::A_BYTES + C::B_BYTES));
+                            tma_load_2d_pair(&args.tmA, bar_c, sm_a + s * C::A_BYTES, k0, tt.m0 + row_off);
+                            tma_load_2d_pair(tmb, bar_c, sm_b + s * C::B_BYTES, k0, tt.n0 + static_cast<int>(rank) * (BN / 2));
                         } else {
-                            mbar_arrive_expect_tx(&ctl->full[s], C::B_BYTES);
+                            if constexpr (!GROUPED) {
+                                mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
+                                tma_load_2d(&args.tmA, &ctl->full[s], sm_a + s * C::A_BYTES, k0, tt.m0);
+                            } else {
+                                mbar_arrive_expect_tx(&ctl->full[s], C::B_BYTES);
+                            }
+                            tma_load_2d(tmb, &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0);
                         }
-                        tma_load_2d(tmb, &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0);
                         trace_event(c, TR_PROD_TMA, it);
                     }
                     if constexpr (GROUPED) {
@@ -466,7 +487,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             }
         }
         // drain: every armed stage's last phase must complete before the CTA exits
-        if (lane == 0) {
+        // (a pair's bytes all complete on the leader's barriers; the final
+        // cluster barrier orders the peer's exit after the leader's drain)
+        if (lane == 0 && leader) {
             for (int d = max(0, it - S); d < it; ++d) {
                 const int sd = d % S;
                 if (sd == withheld) continue;
@@ -487,7 +510,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             if (!ok) break;
             const bool promote = ctl->verdict[v] != 0;
             if (!promote) {
-                if (lane == 0) {
+                if (lane == 0 && leader) {
                     // the accumulator (buffer 0) and, since the scale columns
                     // share its range, buffer 1 must both be drained
                     ok = wait_bar(&ctl->tempty[0], (uses0 & 1u) ^ 1u, ctl, c) &&
@@ -508,25 +531,43 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         const uint32_t sfa = sfa_base + f * C::SF_COLS;
                         const uint32_t sfb = sfa + 4;
                         const uint32_t sf_s = smem_u32(sm_sf + f * C::SF_BYTES);
-                        tmem_cp_32x128b_warpx4(sfa, sdesc_sf_lines(sf_s));
-#pragma unroll
-                        for (int q = 0; q < C::SFB_CHUNKS; ++q)
-                            tmem_cp_32x128b_warpx4(sfb + 4 * q, sdesc_sf_lines(sf_s + 512 * (1 + q)));
                         const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
                         const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
                         const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
+                        if constexpr (PAIR) {
+                            tmem_cp_32x128b_warpx4_pair(sfa, sdesc_sf_lines(sf_s));
 #pragma unroll
-                        for (int j = 0; j < KB_PER_STAGE; ++j) {
-                            if (j < nk)
-                                mma_mxf8(tmem, ad + static_cast<uint64_t>(2 * j), bd + static_cast<uint64_t>(2 * j),
-                                         idesc_mxf8f6f4(BM, BN, j, j), sfa, sfb, (ks | j) != 0 ? 1u : 0u);
+                            for (int q = 0; q < C::SFB_CHUNKS; ++q)
+                                tmem_cp_32x128b_warpx4_pair(sfb + 4 * q, sdesc_sf_lines(sf_s + 512 * (1 + q)));
+#pragma unroll
+                            for (int j = 0; j < KB_PER_STAGE; ++j) {
+                                if (j < nk)
+                                    mma_mxf8_pair(tmem, ad + static_cast<uint64_t>(2 * j), bd + static_cast<uint64_t>(2 * j),
+                                                  idesc_mxf8f6f4(C::TILE_M, BN, j, j), sfa, sfb, (ks | j) != 0 ? 1u : 0u);
+                            }
+                            mma_commit_pair(&ctl->empty[s], PAIR_MASK);
+                            mma_commit_pair(&ctl->sfempty[f], PAIR_MASK);
+                        } else {
+                            tmem_cp_32x128b_warpx4(sfa, sdesc_sf_lines(sf_s));
+#pragma unroll
+                            for (int q = 0; q < C::SFB_CHUNKS; ++q)
+                                tmem_cp_32x128b_warpx4(sfb + 4 * q, sdesc_sf_lines(sf_s + 512 * (1 + q)));
+#pragma unroll
+                            for (int j = 0; j < KB_PER_STAGE; ++j) {
+                                if (j < nk)
+                                    mma_mxf8(tmem, ad + static_cast<uint64_t>(2 * j), bd + static_cast<uint64_t>(2 * j),
+                                             idesc_mxf8f6f4(BM, BN, j, j), sfa, sfb, (ks | j) != 0 ? 1u : 0u);
+                            }
+                            mma_commit(&ctl->empty[s]);
+                            mma_commit(&ctl->sfempty[f]);
                         }
-                        mma_commit(&ctl->empty[s]);
-                        mma_commit(&ctl->sfempty[f]);
                         trace_event(c, TR_MMA_ISSUED, it + ks);
                         issued = true;
                     }
-                    if (ok) mma_commit(&ctl->tfull[0]);
+                    if (ok) {
+                        if constexpr (PAIR) mma_commit_pair(&ctl->tfull[0], PAIR_MASK);
+                        else mma_commit(&ctl->tfull[0]);
+                    }
                 }
                 ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
                 issued = __shfl_sync(FULL, issued ? 1 : 0, 0) != 0;
@@ -538,7 +579,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
                     const int s = it % S;
                     const int f = it % FS;
-                    ok = __all_sync(FULL, wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c) &&
+                    ok = __all_sync(FULL, (!leader || wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c)) &&
                                               wait_bar(&ctl->sfready[f], static_cast<uint32_t>(it / FS) & 1u, ctl, c));
                     if (!ok) break;
                     if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
@@ -559,19 +600,32 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         __syncwarp();
                         if (lane == 0) {
                             mbar_arrive(&ctl->pfull[b]);
-                            tc_fence_after();
-                            mma_f8(tmem + b * BN, ad + static_cast<uint64_t>(2 * j),
-                                   bd + static_cast<uint64_t>(2 * j), idesc_f8f6f4(BM, BN), 0u);
-                            mma_commit(&ctl->tfull[b]);
+                            if (leader) {
+                                tc_fence_after();
+                                if constexpr (PAIR) {
+                                    mma_f8_pair(tmem + b * BN, ad + static_cast<uint64_t>(2 * j),
+                                                bd + static_cast<uint64_t>(2 * j), idesc_f8f6f4(C::TILE_M, BN), 0u);
+                                    mma_commit_pair(&ctl->tfull[b], PAIR_MASK);
+                                } else {
+                                    mma_f8(tmem + b * BN, ad + static_cast<uint64_t>(2 * j),
+                                           bd + static_cast<uint64_t>(2 * j), idesc_f8f6f4(BM, BN), 0u);
+                                    mma_commit(&ctl->tfull[b]);
+                                }
+                            }
                         }
                         issued = true;
                         if (b) { ++uses1; ++pu1; } else { ++uses0; ++pu0; }
                         ++pk;
                     }
                     if (!ok) break;
-                    if (lane == 0) {
-                        mma_commit(&ctl->empty[s]);
-                        mma_commit(&ctl->sfempty[f]);
+                    if (lane == 0 && leader) {
+                        if constexpr (PAIR) {
+                            mma_commit_pair(&ctl->empty[s], PAIR_MASK);
+                            mma_commit_pair(&ctl->sfempty[f], PAIR_MASK);
+                        } else {
+                            mma_commit(&ctl->empty[s]);
+                            mma_commit(&ctl->sfempty[f]);
+                        }
                     }
                     __syncwarp();
                 }
@@ -581,8 +635,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             __syncwarp();
         }
         // all issued tensor-core work must finish before tensor memory is freed
-        if (issued && lane == 0) {
-            mma_commit(&ctl->drain);
+        if (issued && lane == 0 && leader) {
+            if constexpr (PAIR) mma_commit_pair(&ctl->drain, 0x1);
+            else mma_commit(&ctl->drain);
             wait_bar_drain(&ctl->drain, 0u, c.wait_limit);
         }
         __syncwarp();
@@ -595,10 +650,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             if (!ok) break;
             int verdict = 1;
             if (c.mode != PATH_PROMOTE) {
-                const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x));
+                const Tile tt = sch.tile(unit + i * nunits);
                 const GroupEntry e = sch.entry(tt.g);
                 const int MB = (tt.Mg + 31) / 32;
-                const int mb0 = tt.m0 / 32, mb1 = min(mb0 + BM / 32, MB);
+                const int mb0 = tt.m0 / 32, mb1 = min(mb0 + C::TILE_M / 32, MB);
                 const int nb0 = tt.n0 / 32, nb1 = min(nb0 + BN / 32, c.N / 32);
                 bool bad = false;
                 // each tile's scales are two contiguous row ranges of sA and sB
@@ -652,9 +707,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 if (++iks >= c.KS) {   // next tile: per-lane source pointers
                     iks = 0;
                     ++ii;
-                    const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + ii * static_cast<int>(gridDim.x));
+                    const Tile tt = sch.tile(unit + ii * nunits);
                     const GroupEntry e = sch.entry(tt.g);
-                    const int mb = tt.m0 / 32 + (lane >> 2);
+                    const int mb = (tt.m0 + row_off) / 32 + (lane >> 2);
                     const int nb = tt.n0 / 32 + (lane >> 2);
                     a_in = lane < 16 && mb < (tt.Mg + 31) / 32;
                     b_in = lane < 4 * NBB && nb < c.N / 32;
@@ -718,6 +773,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&ctl->sfready[bs]);
+                    if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(&ctl->sfready[bs], 0));
                     trace_event(c, TR_SCALE_READY, it - L);
                     if (bks == c.KS - 1) mbar_arrive(&ctl->vempty[bi & 1]);
                 }
@@ -741,9 +797,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             const bool promote = ctl->verdict[v] != 0;
-            const Tile tt = sch.tile(static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x));
+            const Tile tt = sch.tile(unit + i * nunits);
             const GroupEntry e = sch.entry(tt.g);
-            const int row = tt.m0 + 32 * q + lane;
+            const int row = tt.m0 + row_off + 32 * q + lane;
             const bool row_ok = row < tt.Mg;
             const int col0 = h * C::EPI_COLS;
             __nv_bfloat16 *crow = e.C + static_cast<int64_t>(row_ok ? row : 0) * c.N + tt.n0;
@@ -760,7 +816,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->tempty[0]);
+                if (lane == 0) {
+                    mbar_arrive(&ctl->tempty[0]);
+                    if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(&ctl->tempty[0], 0));
+                }
                 if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_RELEASED, i);
                 ++uses0;
                 if (row_ok) {
@@ -795,7 +854,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         if (x == 2 * NCH - 1) {
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(&ctl->tempty[b]);
+                            if (lane == 0) {
+                                mbar_arrive(&ctl->tempty[b]);
+                                if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(&ctl->tempty[b], 0));
+                            }
                         }
 #pragma unroll
                         for (int y = 0; y < 16; ++y)
@@ -818,22 +880,32 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // no CTA leaves while its peer may still touch its memory
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+        else tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
 template <int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) bsfp8_gemm_plain(const __grid_constant__ PlainArgs args) {
     extern __shared__ uint8_t smem_raw[];
-    gemm_body<BN, false>(args, smem_raw);
+    gemm_body<BN, false, false>(args, smem_raw);
+}
+
+// CTA-pair variant: clusters of two CTAs, 256-row tiles, pair MMAs.
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    bsfp8_gemm_pair(const __grid_constant__ PlainArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    gemm_body<BN, false, true>(args, smem_raw);
 }
 
 template <int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) bsfp8_gemm_grouped(const __grid_constant__ GroupedArgs args) {
     extern __shared__ uint8_t smem_raw[];
-    gemm_body<BN, true>(args, smem_raw);
+    gemm_body<BN, true, false>(args, smem_raw);
 }
 
 // C = 0 for K == 0 (an empty sum).
