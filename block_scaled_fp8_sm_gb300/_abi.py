@@ -47,10 +47,11 @@ class fp8_group_desc(ctypes.Structure):
 _lib = None
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
+def load(path: str = None) -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
+    path = LIB_PATH if path is None else path
     if not os.path.exists(path):
         raise ImportError(
             f"{path} is missing: build it with `python -m block_scaled_fp8_sm_gb300.build` "

@@ -132,12 +132,17 @@ enum : int {
     TR_PROD_TMA = 10,       // producer: stage `it` TMA issued
     TR_PROD_SCALES = 11,    // producer: stage `it` scale copies issued
     TR_PROD_DONE = 12,      // producer: stage `it` completion arrivals registered
-    TR_EVENTS = 13
+    TR_MMA_SF_OK = 13,      // MMA lane 0: scale lines of stage `it` ready
+    TR_MMA_FULL_OK = 14,    // MMA lane 0: own operand bytes of stage `it` landed
+    TR_PEER_FWD = 15,       // peer MMA warp: its bytes of stage `it` landed, forwarded
+    TR_EVENTS = 16
 };
 
+// CTA 1 (the pair peer when CTAs are paired) records at event + TR_EVENTS.
 __device__ __forceinline__ void trace_event(const Common &c, int ev, int idx) {
-    if (c.trace != nullptr && blockIdx.x == 0 && idx >= 0 && idx < TRACE_SLOTS)
-        c.trace[ev * TRACE_SLOTS + idx] = static_cast<unsigned long long>(clock64());
+    if (c.trace != nullptr && blockIdx.x < 2 && idx >= 0 && idx < TRACE_SLOTS)
+        c.trace[(ev + static_cast<int>(blockIdx.x) * TR_EVENTS) * TRACE_SLOTS + idx] =
+            static_cast<unsigned long long>(clock64());
 }
 
 struct PlainArgs {
@@ -157,6 +162,7 @@ template <int STAGES, int SF_STAGES>
 struct Ctrl {
     uint64_t full[STAGES];        // producer -> MMA warp (TMA bytes; grouped: + A-row cp.async)
     uint64_t empty[STAGES];       // MMA commit -> producer
+    uint64_t pfwd[STAGES];        // CTA pairs: peer's stage landed (forwarded to the leader)
     uint64_t scfull[SF_STAGES];   // scale cp.async landed -> scale warp
     uint64_t sfready[SF_STAGES];  // scale warp -> MMA warp (lines written)
     uint64_t sfempty[SF_STAGES];  // MMA commit -> scale warp (lines and scales consumed)
@@ -360,6 +366,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             // arrival per producer lane
             mbar_init(&ctl->full[s], GROUPED ? 1 + 32 : 1);
             mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->pfwd[s], 1);
         }
         for (int f = 0; f < FS; ++f) {
             mbar_init(&ctl->scfull[f], 32);   // one cp.async arrival per scale-warp lane
@@ -450,11 +457,11 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     if (lane == 0) {
                         trace_event(c, TR_PROD_ISSUE, it);
                         if constexpr (PAIR) {
-                            // both CTAs' bytes complete on the leader's barrier
-                            const uint32_t bar_c = mapa_shared(&ctl->full[s], 0);
-                            if (leader) mbar_arrive_expect_tx(&ctl->full[s], 2 * (C::A_BYTES + C::B_BYTES));
-                            tma_load_2d_pair(&args.tmA, bar_c, sm_a + s * C::A_BYTES, k0, tt.m0 + row_off);
-                            tma_load_2d_pair(tmb, bar_c, sm_b + s * C::B_BYTES, k0, tt.n0 + static_cast<int>(rank) * (BN / 2));
+                            // each CTA's bytes complete on its own barrier; the peer's
+                            // MMA warp forwards its completion to the leader
+                            mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
+                            tma_load_2d(&args.tmA, &ctl->full[s], sm_a + s * C::A_BYTES, k0, tt.m0 + row_off);
+                            tma_load_2d(tmb, &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0 + static_cast<int>(rank) * (BN / 2));
                         } else {
                             if constexpr (!GROUPED) {
                                 mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
@@ -487,9 +494,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             }
         }
         // drain: every armed stage's last phase must complete before the CTA exits
-        // (a pair's bytes all complete on the leader's barriers; the final
-        // cluster barrier orders the peer's exit after the leader's drain)
-        if (lane == 0 && leader) {
+        if (lane == 0) {
             for (int d = max(0, it - S); d < it; ++d) {
                 const int sd = d % S;
                 if (sd == withheld) continue;
@@ -523,7 +528,11 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         const uint32_t ph = static_cast<uint32_t>((it + ks) / S) & 1u;
                         const int f = (it + ks) % FS;
                         const uint32_t phf = static_cast<uint32_t>((it + ks) / FS) & 1u;
-                        ok = wait_spin(&ctl->sfready[f], phf, ctl, c) && wait_spin(&ctl->full[s], ph, ctl, c);
+                        ok = wait_spin(&ctl->sfready[f], phf, ctl, c);
+                        trace_event(c, TR_MMA_SF_OK, it + ks);
+                        ok = ok && wait_spin(&ctl->full[s], ph, ctl, c);
+                        trace_event(c, TR_MMA_FULL_OK, it + ks);
+                        ok = ok && (!PAIR || wait_spin(&ctl->pfwd[s], ph, ctl, c));
                         if (!ok) break;
                         trace_event(c, TR_MMA_READY, it + ks);
                         if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
@@ -569,6 +578,19 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         else mma_commit(&ctl->tfull[0]);
                     }
                 }
+                if (PAIR && !leader && lane == 0) {
+                    // forward each stage's scale lines and operand bytes to the
+                    // leader's MMA thread
+                    for (int ks = 0; ks < c.KS && ok; ++ks) {
+                        const int f = (it + ks) % FS;
+                        ok = wait_spin(&ctl->sfready[f], static_cast<uint32_t>((it + ks) / FS) & 1u, ctl, c);
+                        if (ok) mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
+                        const int s = (it + ks) % S;
+                        ok = ok && wait_spin(&ctl->full[s], static_cast<uint32_t>((it + ks) / S) & 1u, ctl, c);
+                        if (ok) mbar_signal_cluster(mapa_shared(&ctl->pfwd[s], 0));
+                        trace_event(c, TR_PEER_FWD, it + ks);
+                    }
+                }
                 ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
                 issued = __shfl_sync(FULL, issued ? 1 : 0, 0) != 0;
                 if (!ok) break;
@@ -579,9 +601,15 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
                     const int s = it % S;
                     const int f = it % FS;
-                    ok = __all_sync(FULL, (!leader || wait_bar(&ctl->full[s], static_cast<uint32_t>(it / S) & 1u, ctl, c)) &&
+                    const uint32_t phs = static_cast<uint32_t>(it / S) & 1u;
+                    ok = __all_sync(FULL, wait_bar(&ctl->full[s], phs, ctl, c) &&
+                                              (!PAIR || !leader || wait_bar(&ctl->pfwd[s], phs, ctl, c)) &&
                                               wait_bar(&ctl->sfready[f], static_cast<uint32_t>(it / FS) & 1u, ctl, c));
                     if (!ok) break;
+                    if (PAIR && !leader && lane == 0) {
+                        mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
+                        mbar_signal_cluster(mapa_shared(&ctl->pfwd[s], 0));
+                    }
                     if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
                     const float *sc = sm_sc + f * C::SC_FLOATS;
                     const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
@@ -702,31 +730,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         uint32_t bph = 0;
         bool promote = false;
         bool ok = true;
+        // each iteration first releases stage it - L, then issues stage it: the
+        // release (cluster scope for a pair) then finds no copy just issued
+        // still in flight
         for (int it = 0; it < total + L && ok; ++it) {
-            if (it < total) {
-                if (++iks >= c.KS) {   // next tile: per-lane source pointers
-                    iks = 0;
-                    ++ii;
-                    const Tile tt = sch.tile(unit + ii * nunits);
-                    const GroupEntry e = sch.entry(tt.g);
-                    const int mb = (tt.m0 + row_off) / 32 + (lane >> 2);
-                    const int nb = tt.n0 / 32 + (lane >> 2);
-                    a_in = lane < 16 && mb < (tt.Mg + 31) / 32;
-                    b_in = lane < 4 * NBB && nb < c.N / 32;
-                    pa = e.sA + (a_in ? static_cast<int64_t>(mb) * c.KB + (lane & 3) : 0);
-                    pb = e.sB + (b_in ? static_cast<int64_t>(nb) * c.KB + (lane & 3) : 0);
-                }
-                ok = __all_sync(FULL, wait_bar(&ctl->sfempty[is], iph ^ 1u, ctl, c));
-                if (!ok) break;
-                const uint32_t sc = smem_u32(sm_sc + is * C::SC_FLOATS);
-                const bool kb_ok = iks * KB_PER_STAGE + (lane & 3) < c.KB;
-                if (lane < 16) cp_async_4(sc + 4 * lane, pa, (a_in && kb_ok) ? 4u : 0u);
-                if (lane < 4 * NBB) cp_async_4(sc + 64 + 4 * lane, pb, (b_in && kb_ok) ? 4u : 0u);
-                cp_async_mbar_arrive_noinc(&ctl->scfull[is]);
-                if (a_in && kb_ok) pa += KB_PER_STAGE;
-                if (b_in && kb_ok) pb += KB_PER_STAGE;
-                if (++is == FS) { is = 0; iph ^= 1u; }
-            }
             if (it >= L) {
                 if (++bks >= c.KS) {   // next tile: its path
                     bks = 0;
@@ -772,13 +779,38 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 if (!promote) fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
+                    // (a pair's peer forwards this to the leader from its MMA warp,
+                    // which has no copies in flight to wait for)
                     mbar_arrive(&ctl->sfready[bs]);
-                    if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(&ctl->sfready[bs], 0));
                     trace_event(c, TR_SCALE_READY, it - L);
                     if (bks == c.KS - 1) mbar_arrive(&ctl->vempty[bi & 1]);
                 }
                 __syncwarp();
                 if (++bs == FS) { bs = 0; bph ^= 1u; }
+            }
+            if (it < total) {
+                if (++iks >= c.KS) {   // next tile: per-lane source pointers
+                    iks = 0;
+                    ++ii;
+                    const Tile tt = sch.tile(unit + ii * nunits);
+                    const GroupEntry e = sch.entry(tt.g);
+                    const int mb = (tt.m0 + row_off) / 32 + (lane >> 2);
+                    const int nb = tt.n0 / 32 + (lane >> 2);
+                    a_in = lane < 16 && mb < (tt.Mg + 31) / 32;
+                    b_in = lane < 4 * NBB && nb < c.N / 32;
+                    pa = e.sA + (a_in ? static_cast<int64_t>(mb) * c.KB + (lane & 3) : 0);
+                    pb = e.sB + (b_in ? static_cast<int64_t>(nb) * c.KB + (lane & 3) : 0);
+                }
+                ok = __all_sync(FULL, wait_bar(&ctl->sfempty[is], iph ^ 1u, ctl, c));
+                if (!ok) break;
+                const uint32_t sc = smem_u32(sm_sc + is * C::SC_FLOATS);
+                const bool kb_ok = iks * KB_PER_STAGE + (lane & 3) < c.KB;
+                if (lane < 16) cp_async_4(sc + 4 * lane, pa, (a_in && kb_ok) ? 4u : 0u);
+                if (lane < 4 * NBB) cp_async_4(sc + 64 + 4 * lane, pb, (b_in && kb_ok) ? 4u : 0u);
+                cp_async_mbar_arrive_noinc(&ctl->scfull[is]);
+                if (a_in && kb_ok) pa += KB_PER_STAGE;
+                if (b_in && kb_ok) pb += KB_PER_STAGE;
+                if (++is == FS) { is = 0; iph ^= 1u; }
             }
         }
         // no scale copy may still be landing when the CTA exits

@@ -163,10 +163,11 @@ int fp8_version(void);
  *   that pipeline stage (counted from 0 over the CTA's whole K loop), so the
  *   waits behind it run out; the output is then incomplete.  -1 (default)
  *   disables it.  Used by the bounded-wait test.
- * FP8_DEBUG_TRACE_BUFFER: device address (0 = off) of a buffer of 13 x 1024
- *   uint64 words; CTA 0 of later launches writes the SM clock of its pipeline
- *   events there (event e, index i at word e*1024 + i).  A profiling aid; the
- *   event numbering is listed with the kernel.
+ * FP8_DEBUG_TRACE_BUFFER: device address (0 = off) of a buffer of
+ *   2 x 16 x 1024 uint64 words; CTAs 0 and 1 of later launches write the SM
+ *   clock of their pipeline events there (CTA b, event e, index i at word
+ *   (b*16 + e)*1024 + i).  A profiling aid; the event numbering is listed
+ *   with the kernel.
  * Returns FP8_OK or FP8_ERR_MODE for an unknown key. */
 enum { FP8_DEBUG_WAIT_LIMIT_CYCLES = 1, FP8_DEBUG_WITHHOLD_STAGE = 2, FP8_DEBUG_TRACE_BUFFER = 3 };
 int fp8_debug_set(int key, int64_t value);
