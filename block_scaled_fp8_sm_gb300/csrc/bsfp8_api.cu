@@ -121,6 +121,24 @@ int encode_kmajor(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int
     return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
 }
 
+// The same K-major matrix seen as {128 K bytes, rows, K/128 halves}: a box
+// {128, box_rows, 2} brings two consecutive 128-K slices of box_rows rows, each
+// 128-byte swizzled, one after the other.  Only whole 128-K slices are in the
+// view (the third extent rounds down), so a box never reaches past a row.
+int encode_kmajor_halves(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
+    const int64_t halves = K / BK > 0 ? K / BK : 1;   // a map with K < 128 is never used
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(halves)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(BK)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 2u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int check_shape(int64_t M, int64_t N, int64_t K) {
@@ -204,6 +222,10 @@ int launch_pair(const void *A, const float *sA, const void *B, const float *sB, 
     int rc = encode_kmajor(&args.tmA, A, M, K, BM);
     if (rc != FP8_OK) return rc;
     rc = encode_kmajor(&args.tmB, B, N, K, BN / 2);
+    if (rc != FP8_OK) return rc;
+    rc = encode_kmajor_halves(&args.tmA3, A, M, K, BM);
+    if (rc != FP8_OK) return rc;
+    rc = encode_kmajor_halves(&args.tmB3, B, N, K, BN / 2);
     if (rc != FP8_OK) return rc;
     args.e.A = static_cast<const uint8_t *>(A);
     args.e.sA = sA;

@@ -78,20 +78,34 @@ struct Cfg {
     static constexpr int BN = BN_;
     static constexpr bool PAIR = PAIR_;   // CTA pair (cta_group::2): 256-row tiles, B split by columns
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;               // output rows per tile
-    static constexpr int STAGES = PAIR ? 6 : ((BN == 256) ? 4 : 6);
-    static constexpr int A_BYTES = BM * BK;                         // this CTA's A rows per stage
-    static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK;       // this CTA's B rows per stage
+    // Wide operand stages (CTA pairs) hold two 128-K halves ([half][rows][128
+    // B], each a 128-byte-swizzled K-major slice) that arrive as one 3D TMA box
+    // per operand: under load the TMA unit's per-request cost dominates, so
+    // fewer, larger requests keep the loads ahead of the tensor cores.  One
+    // scale-ring entry covers one operand stage, so the scale warp and the MMA
+    // thread pay their barrier round trips once per 256 K.
+    static constexpr bool WIDE = PAIR;
+    static constexpr int HALVES = WIDE ? 2 : 1;
+    static constexpr int STAGES = PAIR ? 3 : ((BN == 256) ? 4 : 6);
+    static constexpr int A_HALF = BM * BK;                          // this CTA's A rows, one 128-K half
+    static constexpr int B_HALF = (PAIR ? BN / 2 : BN) * BK;        // this CTA's B rows, one 128-K half
+    static constexpr int A_BYTES = HALVES * A_HALF;                 // per operand stage
+    static constexpr int B_BYTES = HALVES * B_HALF;
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;           // 128 B rows per tcgen05.cp
     static constexpr int SF_BYTES = 512 * (1 + SFB_CHUNKS);         // scale lines per stage
     static constexpr int SF_COLS = 4 * (1 + SFB_CHUNKS);            // tensor-memory columns per stage
-    static constexpr int SF_STAGES = 8;                             // scale ring depth (runs ahead of the operand ring)
-    static constexpr int SF_COL0 = (2 * BN + SF_STAGES * SF_COLS <= 512) ? 2 * BN : BN;
+    static constexpr int SF_STAGES = PAIR ? 9 : 8;                  // scale ring entries (runs ahead of the
+                                                                    // operand ring)
+    static constexpr int SF_ENTRY = HALVES * SF_BYTES;              // lines of one entry
+    static constexpr int SF_ENTRY_COLS = HALVES * SF_COLS;
+    static constexpr int SF_COL0 = (2 * BN + SF_STAGES * SF_ENTRY_COLS <= 512) ? 2 * BN : BN;
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_COLS = BN / 2;                         // columns per epilogue warp
     static constexpr int NBB = BN / 32;                             // 32-column blocks per tile
-    static constexpr int SC_FLOATS = 16 + 4 * NBB;                  // staged fp32 scales per stage
+    static constexpr int SC_FLOATS = 16 + 4 * NBB;                  // staged fp32 scales per 128-K half
+    static constexpr int SC_ENTRY = HALVES * SC_FLOATS;
     static constexpr int PS_FLOATS = 4 * NBB;                       // scale products per K block
-    static_assert(SF_COL0 + SF_STAGES * SF_COLS <= 512 && SF_COL0 >= BN, "tensor memory budget");
+    static_assert(SF_COL0 + SF_STAGES * SF_ENTRY_COLS <= 512 && SF_COL0 >= BN, "tensor memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
     static_assert(4 * NBB <= 32, "one scale product per MMA-warp lane");
 };
@@ -130,8 +144,8 @@ enum : int {
     TR_VERDICT = 8,         // verdict warp: tile `i` published
     TR_MMA_TILE = 9,        // MMA lane 0: tile `i` accumulator free, starting
     TR_PROD_TMA = 10,       // producer: stage `it` TMA issued
-    TR_PROD_SCALES = 11,    // producer: stage `it` scale copies issued
-    TR_PROD_DONE = 12,      // producer: stage `it` completion arrivals registered
+    TR_SCALE_ISSUE = 11,    // scale warp: entry free, issuing the copies of step `it`
+    TR_SCALE_BUILD = 12,    // scale warp: starting step `it`'s lines (before waiting for its copies)
     TR_MMA_SF_OK = 13,      // MMA lane 0: scale lines of stage `it` ready
     TR_MMA_FULL_OK = 14,    // MMA lane 0: own operand bytes of stage `it` landed
     TR_PEER_FWD = 15,       // peer MMA warp: its bytes of stage `it` landed, forwarded
@@ -148,6 +162,8 @@ __device__ __forceinline__ void trace_event(const Common &c, int ev, int idx) {
 struct PlainArgs {
     CUtensorMap tmA;
     CUtensorMap tmB;
+    CUtensorMap tmA3;   // wide stages: {128 K bytes, rows, K/128 halves} views of A and B
+    CUtensorMap tmB3;
     GroupEntry e;
     Common c;
 };
@@ -188,7 +204,7 @@ template <int BN, bool PAIR = false>
 constexpr int smem_bytes() {
     using C = Cfg<BN, PAIR>;
     return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES) +
-           C::SF_STAGES * (C::SF_BYTES + 4 * C::SC_FLOATS) + 2 * 4 * C::PS_FLOATS +
+           C::SF_STAGES * (C::SF_ENTRY + 4 * C::SC_ENTRY) + 2 * 4 * C::PS_FLOATS +
            static_cast<int>(sizeof(Ctrl<C::STAGES, C::SF_STAGES>));
 }
 
@@ -235,6 +251,28 @@ __device__ __forceinline__ bool wait_spin(uint64_t *bar, uint32_t parity, CtrlT 
     }
 }
 
+// Wait of the epilogue warps for a finished accumulator: polls with short
+// sleeps.  A thread parked in try_wait can resume thousands of cycles after the
+// phase completes, and the next tile's MMAs wait for these warps' release.
+template <typename CtrlT>
+__device__ __forceinline__ bool wait_poll(uint64_t *bar, uint32_t parity, CtrlT *ctl,
+                                          const Common &c) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t n = 1;; ++n) {
+        __nanosleep(100);
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((n & 63u) == 0u) {
+            if (*reinterpret_cast<volatile int *>(&ctl->abort)) return false;
+            if (clock64() - t0 > c.wait_limit) {
+                *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
+                atomicOr(c.status, STATUS_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 // Wait used while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ bool wait_bar_drain(uint64_t *bar, uint32_t parity, long long limit) {
     const long long t0 = clock64();
@@ -251,6 +289,7 @@ __device__ __forceinline__ bool is_pow2_scale(float v) {
 }
 
 __device__ __forceinline__ uint32_t ue8m0_of(float v) { return (__float_as_uint(v) >> 23) & 0xFFu; }
+
 
 template <int BN, bool GROUPED, typename Args, int TILE_M = BM>
 struct Sched {
@@ -328,6 +367,25 @@ __device__ __forceinline__ void store_bf16x32f(__nv_bfloat16 *dst, const float *
     }
 }
 
+// One-CTA / CTA-pair forms of the tensor-core issue steps.
+template <bool PAIR>
+__device__ __forceinline__ void cp_lines(uint32_t taddr, uint64_t sdesc) {
+    if constexpr (PAIR) tmem_cp_32x128b_warpx4_pair(taddr, sdesc);
+    else tmem_cp_32x128b_warpx4(taddr, sdesc);
+}
+template <bool PAIR>
+__device__ __forceinline__ void mma_block(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
+                                          uint32_t sfb, uint32_t acc) {
+    if constexpr (PAIR) mma_mxf8_pair(d, ad, bd, idesc, sfa, sfb, acc);
+    else mma_mxf8(d, ad, bd, idesc, sfa, sfb, acc);
+}
+// commit of all earlier tensor-core work to a barrier (both CTAs' copies for a pair)
+template <bool PAIR>
+__device__ __forceinline__ void commit_to(uint64_t *bar) {
+    if constexpr (PAIR) mma_commit_pair(bar, 0x3);
+    else mma_commit(bar);
+}
+
 // ---------------------------------------------------------------------------
 template <int BN, bool GROUPED, bool PAIR, typename Args>
 __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
@@ -342,10 +400,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sm_a = smem;
     uint8_t *sm_b = sm_a + S * C::A_BYTES;
-    uint8_t *sm_sf = sm_b + S * C::B_BYTES;                                  // [FS][SF_BYTES]
+    uint8_t *sm_sf = sm_b + S * C::B_BYTES;                                  // [FS][HALVES][SF_BYTES]
     constexpr int FS = C::SF_STAGES;
-    float *sm_sc = reinterpret_cast<float *>(sm_sf + FS * C::SF_BYTES);      // [FS][SC_FLOATS]
-    float *sm_ps = sm_sc + FS * C::SC_FLOATS;                                  // [2][PS_FLOATS]
+    float *sm_sc = reinterpret_cast<float *>(sm_sf + FS * C::SF_ENTRY);      // [FS][HALVES][SC_FLOATS]
+    float *sm_ps = sm_sc + FS * C::SC_ENTRY;                                   // [2][PS_FLOATS]
     using CtrlT = Ctrl<S, FS>;
     CtrlT *ctl = reinterpret_cast<CtrlT *>(sm_ps + 2 * C::PS_FLOATS);
 
@@ -416,6 +474,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         if constexpr (!GROUPED) {
             tma_prefetch_desc(&args.tmA);
             tma_prefetch_desc(&args.tmB);
+            if constexpr (C::WIDE) {
+                tma_prefetch_desc(&args.tmA3);
+                tma_prefetch_desc(&args.tmB3);
+            }
         }
     }
     tc_fence_before();
@@ -436,10 +498,11 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         // Per stage only: wait for the slot, register the bytes, issue the
         // TMA; tile coordinates are decoded once per tile (a single warp runs
         // dependent integer chains slowly, so the per-stage path stays short).
-        int it = 0, s = 0;
+        int it = 0, s = 0;   // it: operand stages issued (each HALVES x 128 K)
         uint32_t ph = 0;
         int withheld = -1;   // slot never armed (test hook), excluded from the drain
         bool ok = true;
+        const int KW = (c.KS + C::HALVES - 1) / C::HALVES;   // operand stages per tile
         for (int i = 0; i < my_tiles && ok; ++i) {
             const Tile tt = sch.tile(unit + i * nunits);
             const GroupEntry e = sch.entry(tt.g);
@@ -448,7 +511,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             else tmb = &args.tmB;
             const int a_rows = min(BM, tt.Mg - tt.m0);   // grouped: A rows loaded by cp.async
             const uint8_t *a_base = e.A + static_cast<int64_t>(tt.m0) * c.K;
-            for (int ks = 0, k0 = 0; ks < c.KS; ++ks, k0 += BK) {
+            for (int ks = 0, k0 = 0; ks < KW; ++ks, k0 += C::HALVES * BK) {
                 ok = __all_sync(FULL, wait_bar(&ctl->empty[s], ph ^ 1u, ctl, c));
                 if (!ok) break;
                 if ((c.withhold_stage == it) && blockIdx.x == 0) {
@@ -459,9 +522,24 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         if constexpr (PAIR) {
                             // each CTA's bytes complete on its own barrier; the peer's
                             // MMA warp forwards its completion to the leader
-                            mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
-                            tma_load_2d(&args.tmA, &ctl->full[s], sm_a + s * C::A_BYTES, k0, tt.m0 + row_off);
-                            tma_load_2d(tmb, &ctl->full[s], sm_b + s * C::B_BYTES, k0, tt.n0 + static_cast<int>(rank) * (BN / 2));
+                            const int ar = tt.m0 + row_off, br = tt.n0 + static_cast<int>(rank) * (BN / 2);
+                            if (k0 + 2 * BK <= c.K) {
+                                // both halves inside K: one box per operand
+                                mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
+                                tma_load_3d(&args.tmA3, &ctl->full[s], sm_a + s * C::A_BYTES, 0, ar, k0 / BK);
+                                tma_load_3d(&args.tmB3, &ctl->full[s], sm_b + s * C::B_BYTES, 0, br, k0 / BK);
+                            } else {
+                                // the tile's last stage: the halves that start before K,
+                                // from the 2D maps, which zero-fill K past the end
+                                const int nh = k0 + BK < c.K ? 2 : 1;
+                                mbar_arrive_expect_tx(&ctl->full[s], nh * (C::A_HALF + C::B_HALF));
+                                for (int hh = 0; hh < nh; ++hh) {
+                                    tma_load_2d(&args.tmA, &ctl->full[s], sm_a + s * C::A_BYTES + hh * C::A_HALF,
+                                                k0 + hh * BK, ar);
+                                    tma_load_2d(tmb, &ctl->full[s], sm_b + s * C::B_BYTES + hh * C::B_HALF,
+                                                k0 + hh * BK, br);
+                                }
+                            }
                         } else {
                             if constexpr (!GROUPED) {
                                 mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
@@ -503,7 +581,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA warp
-        int it = 0;                       // stage counter (same sequence as the producer)
+        int it = 0;                       // 128-K steps consumed (the scale ring's sequence)
+        int ot = 0;                       // operand stages consumed (the producer's sequence)
+        const int KW = (c.KS + C::HALVES - 1) / C::HALVES;
         uint32_t uses0 = 0, uses1 = 0;    // completed uses of tensor-memory buffers 0 / 1
         uint32_t pk = 0;                  // promotion partials issued (buffer = pk & 1)
         uint32_t pu0 = 0, pu1 = 0;        // promotion uses of buffers 0 / 1 (pfull phases)
@@ -523,97 +603,98 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     trace_event(c, TR_MMA_TILE, i);
                     tc_fence_after();
                     const uint32_t sfa_base = tmem + C::SF_COL0;
-                    for (int ks = 0; ks < c.KS && ok; ++ks) {
-                        const int s = (it + ks) % S;
-                        const uint32_t ph = static_cast<uint32_t>((it + ks) / S) & 1u;
-                        const int f = (it + ks) % FS;
-                        const uint32_t phf = static_cast<uint32_t>((it + ks) / FS) & 1u;
+                    // one pass per operand stage: the MMA pipe holds only about one
+                    // instruction, so the thread keeps the work between MMAs short
+                    // (counters instead of divisions; all scale copies of the stage
+                    // first, then its MMAs back to back)
+                    int s = ot % S, f = ot % FS;
+                    uint32_t ph = static_cast<uint32_t>(ot / S) & 1u, phf = static_cast<uint32_t>(ot / FS) & 1u;
+                    for (int w = 0; w < KW && ok; ++w) {
                         ok = wait_spin(&ctl->sfready[f], phf, ctl, c);
-                        trace_event(c, TR_MMA_SF_OK, it + ks);
+                        trace_event(c, TR_MMA_SF_OK, ot + w);
                         ok = ok && wait_spin(&ctl->full[s], ph, ctl, c);
-                        trace_event(c, TR_MMA_FULL_OK, it + ks);
+                        trace_event(c, TR_MMA_FULL_OK, ot + w);
                         ok = ok && (!PAIR || wait_spin(&ctl->pfwd[s], ph, ctl, c));
                         if (!ok) break;
-                        trace_event(c, TR_MMA_READY, it + ks);
+                        trace_event(c, TR_MMA_READY, ot + w);
                         if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
                         tc_fence_after();
-                        const uint32_t sfa = sfa_base + f * C::SF_COLS;
-                        const uint32_t sfb = sfa + 4;
-                        const uint32_t sf_s = smem_u32(sm_sf + f * C::SF_BYTES);
+                        const uint32_t sfa = sfa_base + f * C::SF_ENTRY_COLS;
+                        const uint32_t sf_s = smem_u32(sm_sf + f * C::SF_ENTRY);
                         const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
                         const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
-                        const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
-                        if constexpr (PAIR) {
-                            tmem_cp_32x128b_warpx4_pair(sfa, sdesc_sf_lines(sf_s));
+                        const int nk = min(C::HALVES * KB_PER_STAGE, c.KB - w * C::HALVES * KB_PER_STAGE);
 #pragma unroll
-                            for (int q = 0; q < C::SFB_CHUNKS; ++q)
-                                tmem_cp_32x128b_warpx4_pair(sfb + 4 * q, sdesc_sf_lines(sf_s + 512 * (1 + q)));
+                        for (int hh = 0; hh < C::HALVES; ++hh) {
+                            if (hh * KB_PER_STAGE < nk) {
+                                cp_lines<PAIR>(sfa + hh * C::SF_COLS, sdesc_sf_lines(sf_s + hh * C::SF_BYTES));
 #pragma unroll
-                            for (int j = 0; j < KB_PER_STAGE; ++j) {
-                                if (j < nk)
-                                    mma_mxf8_pair(tmem, ad + static_cast<uint64_t>(2 * j), bd + static_cast<uint64_t>(2 * j),
-                                                  idesc_mxf8f6f4(C::TILE_M, BN, j, j), sfa, sfb, (ks | j) != 0 ? 1u : 0u);
+                                for (int q = 0; q < C::SFB_CHUNKS; ++q)
+                                    cp_lines<PAIR>(sfa + hh * C::SF_COLS + 4 + 4 * q,
+                                                   sdesc_sf_lines(sf_s + hh * C::SF_BYTES + 512 * (1 + q)));
                             }
-                            mma_commit_pair(&ctl->empty[s], PAIR_MASK);
-                            mma_commit_pair(&ctl->sfempty[f], PAIR_MASK);
-                        } else {
-                            tmem_cp_32x128b_warpx4(sfa, sdesc_sf_lines(sf_s));
-#pragma unroll
-                            for (int q = 0; q < C::SFB_CHUNKS; ++q)
-                                tmem_cp_32x128b_warpx4(sfb + 4 * q, sdesc_sf_lines(sf_s + 512 * (1 + q)));
-#pragma unroll
-                            for (int j = 0; j < KB_PER_STAGE; ++j) {
-                                if (j < nk)
-                                    mma_mxf8(tmem, ad + static_cast<uint64_t>(2 * j), bd + static_cast<uint64_t>(2 * j),
-                                             idesc_mxf8f6f4(BM, BN, j, j), sfa, sfb, (ks | j) != 0 ? 1u : 0u);
-                            }
-                            mma_commit(&ctl->empty[s]);
-                            mma_commit(&ctl->sfempty[f]);
                         }
-                        trace_event(c, TR_MMA_ISSUED, it + ks);
+#pragma unroll
+                        for (int hh = 0; hh < C::HALVES; ++hh) {
+#pragma unroll
+                            for (int j = 0; j < KB_PER_STAGE; ++j) {
+                                if (hh * KB_PER_STAGE + j < nk)
+                                    mma_block<PAIR>(tmem, ad + static_cast<uint64_t>((hh * C::A_HALF >> 4) + 2 * j),
+                                                    bd + static_cast<uint64_t>((hh * C::B_HALF >> 4) + 2 * j),
+                                                    idesc_mxf8f6f4(C::TILE_M, BN, j, j), sfa + hh * C::SF_COLS,
+                                                    sfa + hh * C::SF_COLS + 4, (w | hh | j) != 0 ? 1u : 0u);
+                            }
+                        }
+                        commit_to<PAIR>(&ctl->empty[s]);
+                        commit_to<PAIR>(&ctl->sfempty[f]);
+                        trace_event(c, TR_MMA_ISSUED, ot + w);
                         issued = true;
+                        if (++s == S) { s = 0; ph ^= 1u; }
+                        if (++f == FS) { f = 0; phf ^= 1u; }
                     }
-                    if (ok) {
-                        if constexpr (PAIR) mma_commit_pair(&ctl->tfull[0], PAIR_MASK);
-                        else mma_commit(&ctl->tfull[0]);
-                    }
+                    if (ok) commit_to<PAIR>(&ctl->tfull[0]);
                 }
                 if (PAIR && !leader && lane == 0) {
                     // forward each stage's scale lines and operand bytes to the
                     // leader's MMA thread
-                    for (int ks = 0; ks < c.KS && ok; ++ks) {
-                        const int f = (it + ks) % FS;
-                        ok = wait_spin(&ctl->sfready[f], static_cast<uint32_t>((it + ks) / FS) & 1u, ctl, c);
+                    for (int w = 0; w < KW && ok; ++w) {
+                        const int os = ot + w;
+                        const int f = os % FS;
+                        ok = wait_spin(&ctl->sfready[f], static_cast<uint32_t>(os / FS) & 1u, ctl, c);
                         if (ok) mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
-                        const int s = (it + ks) % S;
-                        ok = ok && wait_spin(&ctl->full[s], static_cast<uint32_t>((it + ks) / S) & 1u, ctl, c);
+                        const int s = os % S;
+                        ok = ok && wait_spin(&ctl->full[s], static_cast<uint32_t>(os / S) & 1u, ctl, c);
                         if (ok) mbar_signal_cluster(mapa_shared(&ctl->pfwd[s], 0));
-                        trace_event(c, TR_PEER_FWD, it + ks);
+                        trace_event(c, TR_PEER_FWD, os);
                     }
                 }
                 ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
                 issued = __shfl_sync(FULL, issued ? 1 : 0, 0) != 0;
                 if (!ok) break;
                 it += c.KS;
+                ot += KW;
                 ++uses0;
             } else {
                 if (pk & 1u) ++pk;   // promotion tiles start on buffer 0 (see the header)
                 for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
-                    const int s = it % S;
-                    const int f = it % FS;
-                    const uint32_t phs = static_cast<uint32_t>(it / S) & 1u;
+                    const int os = ot + ks / C::HALVES;   // operand stage and scale entry; half hh of it
+                    const int hh = ks % C::HALVES;
+                    const bool stage_done = hh == C::HALVES - 1 || ks == c.KS - 1;
+                    const int s = os % S;
+                    const int f = os % FS;
+                    const uint32_t phs = static_cast<uint32_t>(os / S) & 1u;
                     ok = __all_sync(FULL, wait_bar(&ctl->full[s], phs, ctl, c) &&
                                               (!PAIR || !leader || wait_bar(&ctl->pfwd[s], phs, ctl, c)) &&
-                                              wait_bar(&ctl->sfready[f], static_cast<uint32_t>(it / FS) & 1u, ctl, c));
+                                              wait_bar(&ctl->sfready[f], static_cast<uint32_t>(os / FS) & 1u, ctl, c));
                     if (!ok) break;
-                    if (PAIR && !leader && lane == 0) {
+                    if (PAIR && !leader && lane == 0 && hh == 0) {
                         mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
                         mbar_signal_cluster(mapa_shared(&ctl->pfwd[s], 0));
                     }
                     if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
-                    const float *sc = sm_sc + f * C::SC_FLOATS;
-                    const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
-                    const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
+                    const float *sc = sm_sc + f * C::SC_ENTRY + hh * C::SC_FLOATS;
+                    const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES + hh * C::A_HALF));
+                    const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES + hh * C::B_HALF));
                     const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
                     for (int j = 0; j < nk; ++j) {
                         const uint32_t b = pk & 1u;
@@ -647,17 +728,15 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     }
                     if (!ok) break;
                     if (lane == 0 && leader) {
-                        if constexpr (PAIR) {
-                            mma_commit_pair(&ctl->empty[s], PAIR_MASK);
-                            mma_commit_pair(&ctl->sfempty[f], PAIR_MASK);
-                        } else {
-                            mma_commit(&ctl->empty[s]);
-                            mma_commit(&ctl->sfempty[f]);
+                        if (stage_done) {
+                            commit_to<PAIR>(&ctl->empty[s]);
+                            commit_to<PAIR>(&ctl->sfempty[f]);
                         }
                     }
                     __syncwarp();
                 }
                 if (!ok) break;
+                ot += KW;
             }
             if (lane == 0) mbar_arrive(&ctl->vempty[v]);
             __syncwarp();
@@ -712,30 +791,35 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         }
     } else if (warp == 3) {
         // --------------------------------------------------------- scale warp
-        // Loads each stage's fp32 block scales with cp.async (lane l < 16:
-        // sA[m0/32 + l/4][kb0 + l%4]; lane l < 4*BN/32: sB[n0/32 + l/4][kb0 +
-        // l%4]) L stages ahead of turning them into the UE8M0 lines that
-        // tcgen05.cp replicates into all lane quarters.  Absent blocks read as
-        // zero: they only meet discarded rows or K past the end.
-        constexpr int L = 4;
-        const int total = my_tiles * c.KS;
-        // issue side (stage it)
-        int ii = -1, iks = c.KS;            // tile / stage-in-tile of the next issue
+        // One ring entry per operand stage (HALVES x 128 K).  Loads the
+        // entry's fp32 block scales with cp.async -- per half h, lane l < 16:
+        // sA[m0/32 + l/4][kb0 + 4h + l%4]; lane l < 4*BN/32: sB[n0/32 + l/4][kb0
+        // + 4h + l%4] -- L entries ahead of turning them into the UE8M0 lines
+        // that tcgen05.cp replicates into all lane quarters.  Absent blocks read
+        // as zero: they only meet discarded rows or K past the end.  Handling a
+        // whole operand stage per pass pays the barrier round trips once per
+        // 256 K on wide stages.
+        constexpr int H = C::HALVES;
+        constexpr int L = (H == 2) ? 2 : 4;
+        static_assert(L < FS, "scale lookahead");
+        const int KW = (c.KS + H - 1) / H;
+        const int total = my_tiles * KW;
+        // issue side (entry it)
+        int ii = -1, iks = KW;              // tile / stage-in-tile of the next issue
         int is = 0;
         uint32_t iph = 0;
-        const float *pa = nullptr, *pb = nullptr;
+        const float *pa = nullptr, *pb = nullptr;   // this lane's K-block 0 scale of the tile
         bool a_in = false, b_in = false;
-        // build side (stage it - L)
-        int bi = -1, bks = c.KS, bs = 0;
+        // build side (entry it - L)
+        int bi = -1, bks = KW, bs = 0;
         uint32_t bph = 0;
         bool promote = false;
         bool ok = true;
-        // each iteration first releases stage it - L, then issues stage it: the
-        // release (cluster scope for a pair) then finds no copy just issued
-        // still in flight
+        // each iteration first releases entry it - L, then issues entry it: the
+        // release then finds no copy just issued still in flight
         for (int it = 0; it < total + L && ok; ++it) {
             if (it >= L) {
-                if (++bks >= c.KS) {   // next tile: its path
+                if (++bks >= KW) {   // next tile: its path
                     bks = 0;
                     ++bi;
                     const int v = bi & 1;
@@ -743,53 +827,67 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     if (!ok) break;
                     promote = ctl->verdict[v] != 0;
                 }
+                if (lane == 0) trace_event(c, TR_SCALE_BUILD, it - L);
                 ok = __all_sync(FULL, wait_bar(&ctl->scfull[bs], bph, ctl, c));
                 if (!ok) break;
                 if (lane == 0) trace_event(c, TR_SCALE_FULL, it - L);
                 if (!promote) {
-                    // 32 identical 16-byte lines per 128 rows; word w of a line =
-                    // row block w, byte j = K block j of the stage.
-                    const float *sc = sm_sc + bs * C::SC_FLOATS;
-                    const float va = lane < 16 ? sc[lane] : 1.0f;
-                    const float vb = lane < 4 * NBB ? sc[16 + lane] : 1.0f;
-                    uint32_t wa = ue8m0_of(va) << (8 * (lane & 3));
-                    wa |= __shfl_xor_sync(FULL, wa, 1);
-                    wa |= __shfl_xor_sync(FULL, wa, 2);
-                    uint32_t wb = ue8m0_of(vb) << (8 * (lane & 3));
-                    wb |= __shfl_xor_sync(FULL, wb, 1);
-                    wb |= __shfl_xor_sync(FULL, wb, 2);
-                    uint8_t *sf = sm_sf + bs * C::SF_BYTES;
-                    uint4 la;
-                    la.x = __shfl_sync(FULL, wa, 0);
-                    la.y = __shfl_sync(FULL, wa, 4);
-                    la.z = __shfl_sync(FULL, wa, 8);
-                    la.w = __shfl_sync(FULL, wa, 12);
-                    *reinterpret_cast<uint4 *>(sf + lane * 16) = la;
+                    // 32 identical 16-byte lines per 128 rows and half; word w of a
+                    // line = row (column) block w, byte j = K block j of the half.
+                    uint32_t wa[H], wb[H];
 #pragma unroll
-                    for (int q = 0; q < C::SFB_CHUNKS; ++q) {
-                        uint4 lb;
-                        lb.x = __shfl_sync(FULL, wb, 16 * q + 0);
-                        lb.y = __shfl_sync(FULL, wb, 16 * q + 4);
-                        lb.z = __shfl_sync(FULL, wb, 16 * q + 8);
-                        lb.w = __shfl_sync(FULL, wb, 16 * q + 12);
-                        *reinterpret_cast<uint4 *>(sf + 512 * (1 + q) + lane * 16) = lb;
+                    for (int h = 0; h < H; ++h) {
+                        const float *sc = sm_sc + bs * C::SC_ENTRY + h * C::SC_FLOATS;
+                        const float va = lane < 16 ? sc[lane] : 1.0f;
+                        const float vb = lane < 4 * NBB ? sc[16 + lane] : 1.0f;
+                        wa[h] = ue8m0_of(va) << (8 * (lane & 3));
+                        wb[h] = ue8m0_of(vb) << (8 * (lane & 3));
                     }
+#pragma unroll
+                    for (int h = 0; h < H; ++h) {
+                        wa[h] |= __shfl_xor_sync(FULL, wa[h], 1);
+                        wb[h] |= __shfl_xor_sync(FULL, wb[h], 1);
+                    }
+#pragma unroll
+                    for (int h = 0; h < H; ++h) {
+                        wa[h] |= __shfl_xor_sync(FULL, wa[h], 2);
+                        wb[h] |= __shfl_xor_sync(FULL, wb[h], 2);
+                    }
+#pragma unroll
+                    for (int h = 0; h < H; ++h) {
+                        uint8_t *sf = sm_sf + bs * C::SF_ENTRY + h * C::SF_BYTES;
+                        uint4 la;
+                        la.x = __shfl_sync(FULL, wa[h], 0);
+                        la.y = __shfl_sync(FULL, wa[h], 4);
+                        la.z = __shfl_sync(FULL, wa[h], 8);
+                        la.w = __shfl_sync(FULL, wa[h], 12);
+                        *reinterpret_cast<uint4 *>(sf + lane * 16) = la;
+#pragma unroll
+                        for (int q = 0; q < C::SFB_CHUNKS; ++q) {
+                            uint4 lb;
+                            lb.x = __shfl_sync(FULL, wb[h], 16 * q + 0);
+                            lb.y = __shfl_sync(FULL, wb[h], 16 * q + 4);
+                            lb.z = __shfl_sync(FULL, wb[h], 16 * q + 8);
+                            lb.w = __shfl_sync(FULL, wb[h], 16 * q + 12);
+                            *reinterpret_cast<uint4 *>(sf + 512 * (1 + q) + lane * 16) = lb;
+                        }
+                    }
+                    // the lines become visible to tcgen05.cp's async-proxy reads
+                    fence_proxy_async_smem();
                 }
-                // the lines become visible to tcgen05.cp's async-proxy reads
-                if (!promote) fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     // (a pair's peer forwards this to the leader from its MMA warp,
                     // which has no copies in flight to wait for)
                     mbar_arrive(&ctl->sfready[bs]);
                     trace_event(c, TR_SCALE_READY, it - L);
-                    if (bks == c.KS - 1) mbar_arrive(&ctl->vempty[bi & 1]);
+                    if (bks == KW - 1) mbar_arrive(&ctl->vempty[bi & 1]);
                 }
                 __syncwarp();
                 if (++bs == FS) { bs = 0; bph ^= 1u; }
             }
             if (it < total) {
-                if (++iks >= c.KS) {   // next tile: per-lane source pointers
+                if (++iks >= KW) {   // next tile: per-lane source pointers
                     iks = 0;
                     ++ii;
                     const Tile tt = sch.tile(unit + ii * nunits);
@@ -803,13 +901,18 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 }
                 ok = __all_sync(FULL, wait_bar(&ctl->sfempty[is], iph ^ 1u, ctl, c));
                 if (!ok) break;
-                const uint32_t sc = smem_u32(sm_sc + is * C::SC_FLOATS);
-                const bool kb_ok = iks * KB_PER_STAGE + (lane & 3) < c.KB;
-                if (lane < 16) cp_async_4(sc + 4 * lane, pa, (a_in && kb_ok) ? 4u : 0u);
-                if (lane < 4 * NBB) cp_async_4(sc + 64 + 4 * lane, pb, (b_in && kb_ok) ? 4u : 0u);
+                if (lane == 0) trace_event(c, TR_SCALE_ISSUE, it);
+                const uint32_t sc = smem_u32(sm_sc + is * C::SC_ENTRY);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const int kb = (iks * H + h) * KB_PER_STAGE;   // first K block of the half
+                    const bool kb_ok = kb + (lane & 3) < c.KB;
+                    const bool ca = a_in && kb_ok, cb = b_in && kb_ok;
+                    if (lane < 16) cp_async_4(sc + 4 * (h * C::SC_FLOATS + lane), ca ? pa + kb : pa, ca ? 4u : 0u);
+                    if (lane < 4 * NBB)
+                        cp_async_4(sc + 4 * (h * C::SC_FLOATS + 16 + lane), cb ? pb + kb : pb, cb ? 4u : 0u);
+                }
                 cp_async_mbar_arrive_noinc(&ctl->scfull[is]);
-                if (a_in && kb_ok) pa += KB_PER_STAGE;
-                if (b_in && kb_ok) pb += KB_PER_STAGE;
                 if (++is == FS) { is = 0; iph ^= 1u; }
             }
         }
@@ -837,7 +940,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             __nv_bfloat16 *crow = e.C + static_cast<int64_t>(row_ok ? row : 0) * c.N + tt.n0;
 
             if (!promote) {
-                ok = __all_sync(FULL, wait_bar(&ctl->tfull[0], uses0 & 1u, ctl, c));
+                ok = __all_sync(FULL, wait_poll(&ctl->tfull[0], uses0 & 1u, ctl, c));
                 if (!ok) break;
                 if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_FULL, i);
                 tc_fence_after();
@@ -849,8 +952,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
+                    // the loads above have completed (tcgen05.wait::ld), so the
+                    // leader may overwrite the accumulator: a plain signal suffices
                     mbar_arrive(&ctl->tempty[0]);
-                    if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(&ctl->tempty[0], 0));
+                    if (PAIR && !leader) mbar_signal_cluster(mapa_shared(&ctl->tempty[0], 0));
                 }
                 if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_RELEASED, i);
                 ++uses0;
@@ -888,7 +993,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                             __syncwarp();
                             if (lane == 0) {
                                 mbar_arrive(&ctl->tempty[b]);
-                                if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(&ctl->tempty[b], 0));
+                                if (PAIR && !leader) mbar_signal_cluster(mapa_shared(&ctl->tempty[b], 0));
                             }
                         }
 #pragma unroll

@@ -135,6 +135,16 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap *m, uint64_t *bar,
         : "memory");
 }
 
+// Three-dimensional tiled TMA load (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap *m, uint64_t *bar, void *dst,
+                                            int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // ------------------------------------------------------------- tcgen05 ----
 // Allocation is warp-wide (.sync.aligned): all 32 lanes of one warp call it.
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
