@@ -139,6 +139,19 @@ int encode_kmajor_halves(CUtensorMap *m, const void *base, int64_t rows, int64_t
     return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
 }
 
+// bf16 output C (M x N, row-major) for the epilogue's TMA stores: box of
+// STG_COLS columns x BM rows, no swizzle; rows past M are clipped by the TMA.
+int encode_out(CUtensorMap *m, void *C, int64_t M, int64_t N) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2u};
+    const cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(BM)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int check_shape(int64_t M, int64_t N, int64_t K) {
@@ -200,6 +213,8 @@ int launch_plain(const void *A, const float *sA, const void *B, const float *sB,
     if (rc != FP8_OK) return rc;
     rc = encode_kmajor(&args.tmB, B, N, K, BN);
     if (rc != FP8_OK) return rc;
+    rc = encode_out(&args.tmC, C, M, N);
+    if (rc != FP8_OK) return rc;
     args.e.A = static_cast<const uint8_t *>(A);
     args.e.sA = sA;
     args.e.sB = sB;
@@ -222,6 +237,8 @@ int launch_pair(const void *A, const float *sA, const void *B, const float *sB, 
     int rc = encode_kmajor(&args.tmA, A, M, K, BM);
     if (rc != FP8_OK) return rc;
     rc = encode_kmajor(&args.tmB, B, N, K, BN / 2);
+    if (rc != FP8_OK) return rc;
+    rc = encode_out(&args.tmC, C, M, N);
     if (rc != FP8_OK) return rc;
     rc = encode_kmajor_halves(&args.tmA3, A, M, K, BM);
     if (rc != FP8_OK) return rc;
@@ -355,6 +372,8 @@ int launch_plain_noalloc(const void *A, const float *sA, const void *B, const fl
     int rc = encode_kmajor(&args.tmA, A, M, K, BM);
     if (rc != FP8_OK) return rc;
     rc = encode_kmajor(&args.tmB, B, N, K, BN);
+    if (rc != FP8_OK) return rc;
+    rc = encode_out(&args.tmC, C, M, N);
     if (rc != FP8_OK) return rc;
     args.e.A = static_cast<const uint8_t *>(A);
     args.e.sA = sA;

@@ -92,7 +92,8 @@ struct Cfg {
     static constexpr int A_BYTES = HALVES * A_HALF;                 // per operand stage
     static constexpr int B_BYTES = HALVES * B_HALF;
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;           // 128 B rows per tcgen05.cp
-    static constexpr int SF_BYTES = 512 * (1 + SFB_CHUNKS);         // scale lines per stage
+    static constexpr int SF_SET = 128;                              // 8 lines x 16 B, read 4 times by tcgen05.cp
+    static constexpr int SF_BYTES = SF_SET * (1 + SFB_CHUNKS);      // scale lines per 128-K half
     static constexpr int SF_COLS = 4 * (1 + SFB_CHUNKS);            // tensor-memory columns per stage
     static constexpr int SF_STAGES = PAIR ? 9 : 8;                  // scale ring entries (runs ahead of the
                                                                     // operand ring)
@@ -101,6 +102,9 @@ struct Cfg {
     static constexpr int SF_COL0 = (2 * BN + SF_STAGES * SF_ENTRY_COLS <= 512) ? 2 * BN : BN;
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_COLS = BN / 2;                         // columns per epilogue warp
+    // output staging for TMA stores: per column half, BM rows x 32 bf16 columns
+    static constexpr int STG_COLS = 32;
+    static constexpr int STG_BYTES = 2 * BM * STG_COLS * 2;
     static constexpr int NBB = BN / 32;                             // 32-column blocks per tile
     static constexpr int SC_FLOATS = 16 + 4 * NBB;                  // staged fp32 scales per 128-K half
     static constexpr int SC_ENTRY = HALVES * SC_FLOATS;
@@ -149,7 +153,10 @@ enum : int {
     TR_MMA_SF_OK = 13,      // MMA lane 0: scale lines of stage `it` ready
     TR_MMA_FULL_OK = 14,    // MMA lane 0: own operand bytes of stage `it` landed
     TR_PEER_FWD = 15,       // peer MMA warp: its bytes of stage `it` landed, forwarded
-    TR_EVENTS = 16
+    TR_MMA_VOK = 16,        // MMA lane 0: verdict of tile `i` seen
+    TR_MMA_T0 = 17,         // MMA lane 0: accumulator released by the local epilogue (tile `i`)
+    TR_MMA_LOOP = 18,       // MMA lane 0: tile `i`'s K loop about to wait for its first scale entry
+    TR_EVENTS = 24
 };
 
 // CTA 1 (the pair peer when CTAs are paired) records at event + TR_EVENTS.
@@ -162,6 +169,7 @@ __device__ __forceinline__ void trace_event(const Common &c, int ev, int idx) {
 struct PlainArgs {
     CUtensorMap tmA;
     CUtensorMap tmB;
+    CUtensorMap tmC;    // bf16 output {N, M}, box {32, 128}: epilogue TMA stores
     CUtensorMap tmA3;   // wide stages: {128 K bytes, rows, K/128 halves} views of A and B
     CUtensorMap tmB3;
     GroupEntry e;
@@ -203,7 +211,7 @@ struct Tile {
 template <int BN, bool PAIR = false>
 constexpr int smem_bytes() {
     using C = Cfg<BN, PAIR>;
-    return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES) +
+    return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES) + C::STG_BYTES +
            C::SF_STAGES * (C::SF_ENTRY + 4 * C::SC_ENTRY) + 2 * 4 * C::PS_FLOATS +
            static_cast<int>(sizeof(Ctrl<C::STAGES, C::SF_STAGES>));
 }
@@ -353,6 +361,21 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t
     }
 }
 
+// 32 fp32 bit patterns -> 32 bf16 (round to nearest even) into 64 bytes of shared memory.
+__device__ __forceinline__ void pack_bf16x32(uint4 *dst, const uint32_t *r) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t o[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(r[8 * w + 2 * x]),
+                                                      __uint_as_float(r[8 * w + 2 * x + 1]));
+            o[x] = *reinterpret_cast<uint32_t *>(&pr);
+        }
+        dst[w] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 __device__ __forceinline__ void store_bf16x32f(__nv_bfloat16 *dst, const float *v) {
     uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
@@ -400,7 +423,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sm_a = smem;
     uint8_t *sm_b = sm_a + S * C::A_BYTES;
-    uint8_t *sm_sf = sm_b + S * C::B_BYTES;                                  // [FS][HALVES][SF_BYTES]
+    __nv_bfloat16 *sm_stg = reinterpret_cast<__nv_bfloat16 *>(sm_b + S * C::B_BYTES);   // [2][BM][STG_COLS]
+    uint8_t *sm_sf = sm_b + S * C::B_BYTES + C::STG_BYTES;                   // [FS][HALVES][SF_BYTES]
     constexpr int FS = C::SF_STAGES;
     float *sm_sc = reinterpret_cast<float *>(sm_sf + FS * C::SF_ENTRY);      // [FS][HALVES][SC_FLOATS]
     float *sm_ps = sm_sc + FS * C::SC_ENTRY;                                   // [2][PS_FLOATS]
@@ -596,10 +620,12 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             const bool promote = ctl->verdict[v] != 0;
             if (!promote) {
                 if (lane == 0 && leader) {
+                    trace_event(c, TR_MMA_VOK, i);
                     // the accumulator (buffer 0) and, since the scale columns
                     // share its range, buffer 1 must both be drained
-                    ok = wait_bar(&ctl->tempty[0], (uses0 & 1u) ^ 1u, ctl, c) &&
-                         wait_bar(&ctl->tempty[1], (uses1 & 1u) ^ 1u, ctl, c);
+                    ok = wait_bar(&ctl->tempty[0], (uses0 & 1u) ^ 1u, ctl, c);
+                    trace_event(c, TR_MMA_T0, i);
+                    ok = ok && wait_bar(&ctl->tempty[1], (uses1 & 1u) ^ 1u, ctl, c);
                     trace_event(c, TR_MMA_TILE, i);
                     tc_fence_after();
                     const uint32_t sfa_base = tmem + C::SF_COL0;
@@ -609,6 +635,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     // first, then its MMAs back to back)
                     int s = ot % S, f = ot % FS;
                     uint32_t ph = static_cast<uint32_t>(ot / S) & 1u, phf = static_cast<uint32_t>(ot / FS) & 1u;
+                    trace_event(c, TR_MMA_LOOP, i);
                     for (int w = 0; w < KW && ok; ++w) {
                         ok = wait_spin(&ctl->sfready[f], phf, ctl, c);
                         trace_event(c, TR_MMA_SF_OK, ot + w);
@@ -631,7 +658,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 #pragma unroll
                                 for (int q = 0; q < C::SFB_CHUNKS; ++q)
                                     cp_lines<PAIR>(sfa + hh * C::SF_COLS + 4 + 4 * q,
-                                                   sdesc_sf_lines(sf_s + hh * C::SF_BYTES + 512 * (1 + q)));
+                                                   sdesc_sf_lines(sf_s + hh * C::SF_BYTES + C::SF_SET * (1 + q)));
                             }
                         }
 #pragma unroll
@@ -832,8 +859,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 if (!ok) break;
                 if (lane == 0) trace_event(c, TR_SCALE_FULL, it - L);
                 if (!promote) {
-                    // 32 identical 16-byte lines per 128 rows and half; word w of a
-                    // line = row (column) block w, byte j = K block j of the half.
+                    // 8 identical 16-byte lines per 128 rows and half (tcgen05.cp
+                    // reads them four times); word w of a line = row (column) block
+                    // w, byte j = K block j of the half.
                     uint32_t wa[H], wb[H];
 #pragma unroll
                     for (int h = 0; h < H; ++h) {
@@ -861,7 +889,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         la.y = __shfl_sync(FULL, wa[h], 4);
                         la.z = __shfl_sync(FULL, wa[h], 8);
                         la.w = __shfl_sync(FULL, wa[h], 12);
-                        *reinterpret_cast<uint4 *>(sf + lane * 16) = la;
+                        if (lane < 8) *reinterpret_cast<uint4 *>(sf + lane * 16) = la;
 #pragma unroll
                         for (int q = 0; q < C::SFB_CHUNKS; ++q) {
                             uint4 lb;
@@ -869,7 +897,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                             lb.y = __shfl_sync(FULL, wb[h], 16 * q + 4);
                             lb.z = __shfl_sync(FULL, wb[h], 16 * q + 8);
                             lb.w = __shfl_sync(FULL, wb[h], 16 * q + 12);
-                            *reinterpret_cast<uint4 *>(sf + 512 * (1 + q) + lane * 16) = lb;
+                            if (lane < 8) *reinterpret_cast<uint4 *>(sf + C::SF_SET * (1 + q) + lane * 16) = lb;
                         }
                     }
                     // the lines become visible to tcgen05.cp's async-proxy reads
@@ -926,10 +954,22 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         constexpr int NCH = C::EPI_COLS / 32;         // 32-column chunks per warp
         uint32_t uses0 = 0, uses1 = 0, pk = 0;
         uint32_t pu0 = 0, pu1 = 0;   // promotion uses of buffers 0 / 1 (pfull phases)
+        // Single problems write native tiles through shared memory with TMA
+        // stores: one lane per output row would otherwise flood the load/store
+        // path with row-scattered stores for thousands of cycles, and the MMA
+        // thread's barrier operations queue behind them.  The four warps of a
+        // column half share a staging buffer and a named barrier; every exit
+        // from the loop is agreed among them first (named_bar_and), so no warp
+        // is ever left waiting at that barrier.
+        constexpr bool TMA_OUT = !GROUPED;
+        const uint32_t bar_id = 1u + static_cast<uint32_t>(h);
+        constexpr uint32_t HALF_THREADS = 128;
+        const bool issuer = q == 0 && lane == 0;
         for (int i = 0; i < my_tiles; ++i) {
             const int v = i & 1;
             bool ok = wait_bar(&ctl->vfull[v], static_cast<uint32_t>(i >> 1) & 1u, ctl, c);
             ok = __all_sync(FULL, ok);
+            if constexpr (TMA_OUT) ok = named_bar_and(bar_id, HALF_THREADS, ok);
             if (!ok) break;
             const bool promote = ctl->verdict[v] != 0;
             const Tile tt = sch.tile(unit + i * nunits);
@@ -941,6 +981,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 
             if (!promote) {
                 ok = __all_sync(FULL, wait_poll(&ctl->tfull[0], uses0 & 1u, ctl, c));
+                if constexpr (TMA_OUT) ok = named_bar_and(bar_id, HALF_THREADS, ok);
                 if (!ok) break;
                 if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_FULL, i);
                 tc_fence_after();
@@ -959,7 +1000,27 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 }
                 if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_RELEASED, i);
                 ++uses0;
-                if (row_ok) {
+                if constexpr (TMA_OUT) {
+                    // 32-column chunks: rows into the half's staging buffer, then
+                    // one TMA store of the 128 x 32 box (rows past M are clipped)
+                    __nv_bfloat16 *stg = sm_stg + h * (BM * C::STG_COLS);
+                    uint4 *mine = reinterpret_cast<uint4 *>(stg + (32 * q + lane) * C::STG_COLS);
+#pragma unroll
+                    for (int x = 0; x < NCH; ++x) {
+                        pack_bf16x32(mine, r[x]);
+                        fence_proxy_async_smem();
+                        named_bar_sync(bar_id, HALF_THREADS);
+                        if (issuer) {
+                            const int col = tt.n0 + col0 + 32 * x;
+                            if (col < c.N) {
+                                tma_store_2d(&args.tmC, stg, col, tt.m0 + row_off);
+                                bulk_commit_group();
+                                bulk_wait_read_all();
+                            }
+                        }
+                        named_bar_sync(bar_id, HALF_THREADS);   // the buffer is free again
+                    }
+                } else if (row_ok) {
 #pragma unroll
                     for (int x = 0; x < NCH; ++x)
                         if (tt.n0 + col0 + 32 * x < c.N) store_bf16x32(crow + col0 + 32 * x, r[x]);
@@ -977,6 +1038,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     ok = wait_bar(&ctl->pfull[b], pb & 1u, ctl, c) &&
                          wait_bar(&ctl->tfull[b], ub & 1u, ctl, c);
                     ok = __all_sync(FULL, ok);
+                    if constexpr (TMA_OUT) ok = named_bar_and(bar_id, HALF_THREADS, ok);
                     if (!ok) break;
                     tc_fence_after();
                     float sc[NCH];
@@ -1013,6 +1075,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->vempty[v]);
         }
+        if (TMA_OUT && issuer) bulk_wait_all();   // the output is written before the CTA exits
     }
 
     tc_fence_before();

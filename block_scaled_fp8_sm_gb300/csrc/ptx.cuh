@@ -135,6 +135,36 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap *m, uint64_t *bar,
         : "memory");
 }
 
+// Two-dimensional tiled TMA store from shared memory (bulk-group completion);
+// elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *src, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of all committed bulk stores have been read
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all committed bulk stores have completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Named barrier over `count` threads (warp multiples).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also returns the AND of every participant's predicate.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0u;
+}
+
 // Three-dimensional tiled TMA load (coordinates innermost first).
 __device__ __forceinline__ void tma_load_3d(const CUtensorMap *m, uint64_t *bar, void *dst,
                                             int32_t c0, int32_t c1, int32_t c2) {
@@ -262,11 +292,12 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
 }
 
 // Descriptor of a 32-row x 16-byte source for tcgen05.cp (no swizzle; rows of
-// 16 bytes back to back, 8-row groups 128 bytes apart).
+// 16 bytes back to back within an 8-row group).  The stride between 8-row
+// groups is zero: the scale lines are identical for all 32 rows, so one
+// 128-byte group of 8 lines is read four times.
 __device__ __forceinline__ uint64_t sdesc_sf_lines(uint32_t saddr) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(128u >> 4) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
     return d;
 }

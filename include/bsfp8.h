@@ -164,9 +164,9 @@ int fp8_version(void);
  *   waits behind it run out; the output is then incomplete.  -1 (default)
  *   disables it.  Used by the bounded-wait test.
  * FP8_DEBUG_TRACE_BUFFER: device address (0 = off) of a buffer of
- *   2 x 16 x 1024 uint64 words; CTAs 0 and 1 of later launches write the SM
+ *   2 x 24 x 1024 uint64 words; CTAs 0 and 1 of later launches write the SM
  *   clock of their pipeline events there (CTA b, event e, index i at word
- *   (b*16 + e)*1024 + i).  A profiling aid; the event numbering is listed
+ *   (b*24 + e)*1024 + i).  A profiling aid; the event numbering is listed
  *   with the kernel.
  * Returns FP8_OK or FP8_ERR_MODE for an unknown key. */
 enum { FP8_DEBUG_WAIT_LIMIT_CYCLES = 1, FP8_DEBUG_WITHHOLD_STAGE = 2, FP8_DEBUG_TRACE_BUFFER = 3 };
