@@ -198,6 +198,7 @@ struct Ctrl {
     uint64_t drain;
     uint32_t tmem_base;
     int verdict[2];
+    int first_bad;              // the CTA's first tile reads a non-power-of-two scale
     int abort;
     int num_tiles;
     int tile_start[MAX_GROUPS + 1];
@@ -345,6 +346,35 @@ struct Sched {
     }
 };
 
+// True when any scale the tile reads is not a positive normal power of two.
+// The tile's scales are two contiguous ranges (sA rows mb0..mb1 and sB rows
+// nb0..nb1, all K blocks); thread t of n scans elements t, t + n, ..., with
+// 16 loads in flight per round (the first tile's scan is a cold DRAM read).
+template <int BN, int TILE_M>
+__device__ __forceinline__ bool tile_has_bad_scale(const Tile &tt, const GroupEntry &e, const Common &c,
+                                                   int t, int n) {
+    const int MB = (tt.Mg + 31) / 32;
+    const int mb0 = tt.m0 / 32, mb1 = min(mb0 + TILE_M / 32, MB);
+    const int nb0 = tt.n0 / 32, nb1 = min(nb0 + BN / 32, c.N / 32);
+    const float *pa = e.sA + static_cast<int64_t>(mb0) * c.KB;
+    const int na = (mb1 - mb0) * c.KB;
+    const float *pb = e.sB + static_cast<int64_t>(nb0) * c.KB;
+    const int total = na + (nb1 - nb0) * c.KB;
+    constexpr int U = 16;
+    bool bad = false;
+    for (int x0 = t; x0 < total; x0 += n * U) {
+        float v[U];
+#pragma unroll
+        for (int w = 0; w < U; ++w) {
+            const int x = x0 + w * n;
+            v[w] = x < na ? __ldg(pa + x) : (x < total ? __ldg(pb + (x - na)) : 1.0f);
+        }
+#pragma unroll
+        for (int w = 0; w < U; ++w) bad |= !is_pow2_scale(v[w]);
+    }
+    return bad;
+}
+
 // 32 consecutive bf16 outputs (64 bytes, 16-byte aligned) from fp32 bits / values.
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t *r) {
     uint4 *d = reinterpret_cast<uint4 *>(dst);
@@ -464,6 +494,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         }
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
+        ctl->first_bad = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -516,6 +547,20 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     if constexpr (!GROUPED) e0 = args.e;
     const Sched<BN, GROUPED, Args, C::TILE_M> sch{args, c, ctl->tile_start, ctl->mg, e0};
     constexpr uint16_t PAIR_MASK = 0x3;
+
+    // The first tile's path verdict gates its MMAs and its scale lines.  Warps
+    // 1..11 compute it together (one or two rounds of loads instead of the
+    // verdict warp's many) while the producer warp starts loading operands.
+    if (warp != 0) {
+        bool bad = false;
+        if (my_tiles > 0 && c.mode != PATH_PROMOTE) {
+            const Tile tt = sch.tile(unit);
+            bad = tile_has_bad_scale<BN, C::TILE_M>(tt, sch.entry(tt.g), c, threadIdx.x - 32,
+                                                    NUM_THREADS - 32);
+        }
+        if (__any_sync(FULL, bad) && lane == 0) atomicOr(&ctl->first_bad, 1);
+        named_bar_sync(1, NUM_THREADS - 32);
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -784,28 +829,13 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             if (!ok) break;
             int verdict = 1;
             if (c.mode != PATH_PROMOTE) {
-                const Tile tt = sch.tile(unit + i * nunits);
-                const GroupEntry e = sch.entry(tt.g);
-                const int MB = (tt.Mg + 31) / 32;
-                const int mb0 = tt.m0 / 32, mb1 = min(mb0 + C::TILE_M / 32, MB);
-                const int nb0 = tt.n0 / 32, nb1 = min(nb0 + BN / 32, c.N / 32);
-                bool bad = false;
-                // each tile's scales are two contiguous row ranges of sA and sB
-                const float *pa = e.sA + static_cast<int64_t>(mb0) * c.KB;
-                const int na = (mb1 - mb0) * c.KB;
-                const float *pb = e.sB + static_cast<int64_t>(nb0) * c.KB;
-                const int nbn = (nb1 - nb0) * c.KB;
-                for (int x = lane; x < na; x += 32 * 8) {
-#pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        if (x + 32 * w < na) bad |= !is_pow2_scale(__ldg(pa + x + 32 * w));
+                bool any_bad;
+                if (i == 0) {
+                    any_bad = ctl->first_bad != 0;   // computed by warps 1..11 at the start
+                } else {
+                    const Tile tt = sch.tile(unit + i * nunits);
+                    any_bad = __any_sync(FULL, tile_has_bad_scale<BN, C::TILE_M>(tt, sch.entry(tt.g), c, lane, 32));
                 }
-                for (int x = lane; x < nbn; x += 32 * 8) {
-#pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        if (x + 32 * w < nbn) bad |= !is_pow2_scale(__ldg(pb + x + 32 * w));
-                }
-                const bool any_bad = __any_sync(FULL, bad);
                 verdict = any_bad ? 1 : 0;
                 if (any_bad && c.mode == PATH_NATIVE && lane == 0) atomicOr(c.status, STATUS_SCALE);
             }
