@@ -525,14 +525,18 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             if (lane == 0) ctl->num_tiles = c.num_tiles;
         }
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
         if constexpr (!GROUPED) {
-            tma_prefetch_desc(&args.tmA);
-            tma_prefetch_desc(&args.tmB);
-            if constexpr (C::WIDE) {
-                tma_prefetch_desc(&args.tmA3);
-                tma_prefetch_desc(&args.tmB3);
+            if (lane == 0) {
+                tma_prefetch_desc(&args.tmA);
+                tma_prefetch_desc(&args.tmB);
+                if constexpr (C::WIDE) {
+                    tma_prefetch_desc(&args.tmA3);
+                    tma_prefetch_desc(&args.tmB3);
+                }
             }
+        } else {
+            for (int g = lane; g < c.G; g += 32) tma_prefetch_desc(&args.tmB[g]);
         }
     }
     tc_fence_before();
@@ -548,18 +552,20 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     const Sched<BN, GROUPED, Args, C::TILE_M> sch{args, c, ctl->tile_start, ctl->mg, e0};
     constexpr uint16_t PAIR_MASK = 0x3;
 
-    // The first tile's path verdict gates its MMAs and its scale lines.  Warps
-    // 1..11 compute it together (one or two rounds of loads instead of the
-    // verdict warp's many) while the producer warp starts loading operands.
-    if (warp != 0) {
+    // The first tile's path verdict gates its MMAs and its scale lines.  Ten
+    // warps compute it together (one or two rounds of loads instead of the
+    // verdict warp's many) while the producer warp starts loading operands and
+    // the scale warp its first scale copies.
+    if (warp != 0 && warp != 3) {
+        constexpr int SCANNERS = NUM_THREADS - 64;
         bool bad = false;
         if (my_tiles > 0 && c.mode != PATH_PROMOTE) {
             const Tile tt = sch.tile(unit);
-            bad = tile_has_bad_scale<BN, C::TILE_M>(tt, sch.entry(tt.g), c, threadIdx.x - 32,
-                                                    NUM_THREADS - 32);
+            const int t = static_cast<int>(threadIdx.x) - (warp < 3 ? 32 : 64);
+            bad = tile_has_bad_scale<BN, C::TILE_M>(tt, sch.entry(tt.g), c, t, SCANNERS);
         }
         if (__any_sync(FULL, bad) && lane == 0) atomicOr(&ctl->first_bad, 1);
-        named_bar_sync(1, NUM_THREADS - 32);
+        named_bar_sync(1, SCANNERS);
     }
 
     if (warp == 0) {
