@@ -209,6 +209,52 @@ def time_device(run, steps, warmup, dev, flush_buf, world):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def time_graph_grouped(steps, warmup, dev, bs, flush_buf):
+    """The grouped-decode launch captured once in a CUDA graph: device time per
+    replay (same L2 flush between steps) and host time per launch, direct call
+    versus replay (the direct call encodes one tensor map per group)."""
+    import torch
+
+    import workloads
+    p = workloads.make("c3", seed=0, device=dev)
+    Cs = [torch.empty(m, p.N, dtype=torch.bfloat16, device=dev) for m in p.Ms]
+    groups = [(p.A[o:o + m], sa, b, sb, c) for o, m, sa, b, sb, c in
+              zip(p.offsets, p.Ms, p.sA, p.B, p.sB, Cs)]
+    Ms = torch.tensor(p.Ms, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    bs.fp8_gemm_grouped(groups, Ms, p.N, p.K)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        bs.fp8_gemm_grouped(groups, Ms, p.N, p.K)
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        flush_buf.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+
+    def host_us(fn, n=20):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize(dev)
+        return (t1 - t0) / n * 1e6
+    direct = host_us(lambda: bs.fp8_gemm_grouped(groups, Ms, p.N, p.K))
+    replay = host_us(graph.replay)
+    del graph
+    return {"ms_per_step": round(ms, 4), "value": round(p.algorithmic_bytes / (ms * 1e-3) / 1e9, 1),
+            "unit": "GB/s", "host_us_per_launch": {"direct": round(direct, 1), "graph_replay": round(replay, 1)}}
+
+
 def time_e2e(name, steps, warmup, dev, bs, world):
     """Same metric through the public API with pinned HOST buffers: each step
     copies the inputs host->device, runs the GEMM and reads C back."""
@@ -317,6 +363,8 @@ def run_ours(args):
                               "gbs": r["bytes"] / (r["ms"] * 1e-3) / 1e9}))
         return
     e2e = time_e2e(HEADLINE, max(3, args.steps // 5), args.warmup, dev, bs, world)
+    graph_c3 = (time_graph_grouped(args.steps, args.warmup, dev, bs, flush)
+                if "c3" in names and world == 1 else None)
 
     if rank != 0:
         return
@@ -345,6 +393,8 @@ def run_ours(args):
             entry["value"] = round(r["bytes"] / (r["ms"] * 1e-3) / 1e9, 1)
             entry["unit"] = "GB/s"
             entry["algorithmic_bytes"] = r["bytes"]
+            if graph_c3:
+                entry["graph_replay"] = graph_c3
         else:
             entry["value"] = round(r["flops"] / (r["ms"] * 1e-3) / 1e12, 1)
             entry["unit"] = "TFLOP/s"
@@ -367,7 +417,9 @@ def run_ours(args):
                    "l2": "flushed between timed steps (512 MiB write)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline(HEADLINE),
-        "gpu_launches": args.steps * len(names),
+        # launches of this library's kernels inside timed regions: every timed
+        # step of every workload, the graph replays and the end-to-end steps
+        "gpu_launches": args.steps * len(names) + (args.steps if graph_c3 else 0) + max(3, args.steps // 5),
         "clocks": clk.summary(),
         "extra": extra,
     }

@@ -16,11 +16,18 @@ def bf16_to_f64(c: torch.Tensor) -> np.ndarray:
     return c.float().cpu().numpy().astype(np.float64)
 
 
+# what -> (worst, mean, elements) of |C - C_ref| / bound, for the session summary
+REPORT: dict = {}
+
+
 def check(C_gpu: np.ndarray, C_ref: np.ndarray, T: np.ndarray, what: str = ""):
     err = np.abs(C_gpu - C_ref)
     bound = REL * np.abs(C_ref) + ABS_T * T
     bad = ~(err <= bound)
-    ratio = float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
+    r = err / np.maximum(bound, 1e-300)
+    ratio = float(np.max(r)) if err.size else 0.0
+    if err.size:
+        REPORT[what] = (ratio, float(np.mean(r)), int(err.size))
     if bad.any():
         idx = np.argwhere(bad)[:5]
         msg = [f"{what}: {int(bad.sum())}/{bad.size} elements outside the bound; worst ratio {ratio:.3g}"]

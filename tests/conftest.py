@@ -24,3 +24,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Worst and mean |C - C_ref| / bound of every parity comparison made."""
+    try:
+        from tests._accept import REPORT
+    except Exception:  # pragma: no cover
+        return
+    if not REPORT:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "parity margins: |C - C_ref| / (4e-3*|C_ref| + 1e-5*T)")
+    tr.write_line(f"{'case':44s} {'worst':>8s} {'mean':>9s} {'elements':>10s}")
+    for what, (worst, mean, n) in REPORT.items():
+        tr.write_line(f"{what[:44]:44s} {worst:8.3f} {mean:9.4f} {n:10d}")
