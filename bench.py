@@ -249,10 +249,13 @@ def time_graph_grouped(steps, warmup, dev, bs, flush_buf):
         torch.cuda.synchronize(dev)
         return (t1 - t0) / n * 1e6
     direct = host_us(lambda: bs.fp8_gemm_grouped(groups, Ms, p.N, p.K))
+    descs = bs.group_descs(groups)
+    prebuilt = host_us(lambda: bs.fp8_gemm_grouped(descs, Ms, p.N, p.K))
     replay = host_us(graph.replay)
     del graph
     return {"ms_per_step": round(ms, 4), "value": round(p.algorithmic_bytes / (ms * 1e-3) / 1e9, 1),
-            "unit": "GB/s", "host_us_per_launch": {"direct": round(direct, 1), "graph_replay": round(replay, 1)}}
+            "unit": "GB/s", "host_us_per_launch": {"direct": round(direct, 1), "prebuilt_descs": round(prebuilt, 1),
+                                   "graph_replay": round(replay, 1)}}
 
 
 def time_e2e(name, steps, warmup, dev, bs, world):

@@ -15,8 +15,9 @@ from ._abi import (FP8_PATH_AUTO, FP8_PATH_NATIVE, FP8_PATH_PROMOTE,  # noqa: F4
                    FP8_DEBUG_WAIT_LIMIT_CYCLES, FP8_DEBUG_WITHHOLD_STAGE, FP8_DEBUG_TRACE_BUFFER,
                    FP8_MAX_GROUPS_PER_LAUNCH, fp8_group_desc)
 
-__all__ = ["fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_gemm_grouped", "fp8_status_query", "fp8_strerror",
-           "fp8_version", "fp8_debug_set", "fp8_lib_shutdown", "Fp8Error", "library"]
+__all__ = ["fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_gemm_grouped", "group_descs",
+           "fp8_status_query", "fp8_strerror", "fp8_version", "fp8_debug_set", "fp8_lib_shutdown",
+           "Fp8Error", "library"]
 
 
 class Fp8Error(RuntimeError):
@@ -80,13 +81,35 @@ def fp8_gemm_blockscaled_noalloc(A, sA, B, sB, C, M=None, N=None, K=None, stream
     return C
 
 
+class GroupDescs:
+    """The host array of per-group pointer records that fp8_gemm_grouped
+    takes, built once (the tensors stay referenced) so that repeated calls on
+    the same buffers skip the per-call pointer marshalling."""
+
+    def __init__(self, groups):
+        self.groups = list(groups)
+        self.G = len(self.groups)
+        self.arr = (fp8_group_desc * max(self.G, 1))()
+        for g, (a, sa, b, sb, c) in enumerate(self.groups):
+            self.arr[g] = fp8_group_desc(*[x if isinstance(x, int) else _ptr(x) for x in (a, sa, b, sb, c)])
+
+
+def group_descs(groups) -> GroupDescs:
+    return GroupDescs(groups)
+
+
 def fp8_gemm_grouped(groups, Ms, N, K, G=None, stream=None, mode=None):
     """groups: sequence of (A_g, sA_g, B_g, sB_g, C_g) CUDA tensors (or raw
-    device pointers); Ms: int32 CUDA tensor of G row counts (read on device)."""
-    G = len(groups) if G is None else G
-    arr = (fp8_group_desc * max(G, 1))()
-    for g, (a, sa, b, sb, c) in enumerate(groups[:G]):
-        arr[g] = fp8_group_desc(*[x if isinstance(x, int) else _ptr(x) for x in (a, sa, b, sb, c)])
+    device pointers), or a GroupDescs built from one; Ms: int32 CUDA tensor of
+    G row counts (read on device)."""
+    if isinstance(groups, GroupDescs):
+        G = groups.G if G is None else G
+        arr = groups.arr
+    else:
+        G = len(groups) if G is None else G
+        arr = (fp8_group_desc * max(G, 1))()
+        for g, (a, sa, b, sb, c) in enumerate(groups[:G]):
+            arr[g] = fp8_group_desc(*[x if isinstance(x, int) else _ptr(x) for x in (a, sa, b, sb, c)])
     lib = library()
     s = _stream(stream)
     ms = Ms if isinstance(Ms, int) else _ptr(Ms)

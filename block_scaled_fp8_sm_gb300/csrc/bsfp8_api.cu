@@ -8,6 +8,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "bsfp8.h"
 #include "gemm_kernel.cuh"
@@ -109,7 +110,7 @@ int device_setup(DeviceState **out) {
 }
 
 // 2-D K-major byte tensor [rows, K] with a (BK x box_rows) box, 128-byte swizzle.
-int encode_kmajor(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
+int encode_kmajor_raw(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
@@ -125,7 +126,7 @@ int encode_kmajor(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int
 // {128, box_rows, 2} brings two consecutive 128-K slices of box_rows rows, each
 // 128-byte swizzled, one after the other.  Only whole 128-K slices are in the
 // view (the third extent rounds down), so a box never reaches past a row.
-int encode_kmajor_halves(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
+int encode_kmajor_halves_raw(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
     const int64_t halves = K / BK > 0 ? K / BK : 1;   // a map with K < 128 is never used
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(halves)};
@@ -141,7 +142,7 @@ int encode_kmajor_halves(CUtensorMap *m, const void *base, int64_t rows, int64_t
 
 // bf16 output C (M x N, row-major) for the epilogue's TMA stores: box of
 // STG_COLS columns x BM rows, no swizzle; rows past M are clipped by the TMA.
-int encode_out(CUtensorMap *m, void *C, int64_t M, int64_t N) {
+int encode_out_raw(CUtensorMap *m, void *C, int64_t M, int64_t N) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2u};
     const cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(BM)};
@@ -150,6 +151,61 @@ int encode_out(CUtensorMap *m, void *C, int64_t M, int64_t N) {
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
+// A tensor map is a pure function of its encode arguments, so one cached by
+// those arguments stays valid whatever later happens to the memory behind it.
+// The cache saves the host ~2 us per map (a grouped call encodes one per group).
+struct MapKey {
+    int kind;   // 0: 2D K-major, 1: 3D K-major halves, 2: bf16 output
+    int box;
+    const void *base;
+    int64_t a, b;
+    bool operator==(const MapKey &o) const {
+        return kind == o.kind && box == o.box && base == o.base && a == o.a && b == o.b;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const {
+        uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+        h ^= static_cast<uint64_t>(k.a) + 0x632BE59BD9B4E019ull + (h << 6) + (h >> 2);
+        h ^= static_cast<uint64_t>(k.b) + 0x85157AF5ull + (h << 6) + (h >> 2);
+        h ^= static_cast<uint64_t>(k.kind * 1024 + k.box) + (h << 6) + (h >> 2);
+        return static_cast<size_t>(h);
+    }
+};
+constexpr size_t kMaxCachedMaps = 4096;
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+template <typename Encode>
+int cached_map(CUtensorMap *m, const MapKey &k, Encode encode) {
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_maps.find(k);
+        if (it != g_maps.end()) {
+            *m = it->second;
+            return FP8_OK;
+        }
+    }
+    const int rc = encode(m);
+    if (rc != FP8_OK) return rc;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
+    g_maps.emplace(k, *m);
+    return FP8_OK;
+}
+
+int encode_kmajor(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
+    return cached_map(m, MapKey{0, box_rows, base, rows, K},
+                      [&](CUtensorMap *o) { return encode_kmajor_raw(o, base, rows, K, box_rows); });
+}
+int encode_kmajor_halves(CUtensorMap *m, const void *base, int64_t rows, int64_t K, int box_rows) {
+    return cached_map(m, MapKey{1, box_rows, base, rows, K},
+                      [&](CUtensorMap *o) { return encode_kmajor_halves_raw(o, base, rows, K, box_rows); });
+}
+int encode_out(CUtensorMap *m, void *C, int64_t M, int64_t N) {
+    return cached_map(m, MapKey{2, BM, C, M, N}, [&](CUtensorMap *o) { return encode_out_raw(o, C, M, N); });
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -535,6 +591,8 @@ void fp8_lib_shutdown(void) {
         }
         g_dev[i] = DeviceState();
     }
+    std::lock_guard<std::mutex> lm(g_map_mu);
+    g_maps.clear();
 }
 
 }  // extern "C"

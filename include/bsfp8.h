@@ -172,7 +172,9 @@ int fp8_version(void);
 enum { FP8_DEBUG_WAIT_LIMIT_CYCLES = 1, FP8_DEBUG_WITHHOLD_STAGE = 2, FP8_DEBUG_TRACE_BUFFER = 3 };
 int fp8_debug_set(int key, int64_t value);
 
-/* Frees the per-device status words.  Later calls set them up again. */
+/* Frees the per-device status words and empties the host cache of TMA
+ * descriptors (each is a pure function of a call's pointers and sizes, so the
+ * cache never holds a stale one).  Later calls set both up again. */
 void fp8_lib_shutdown(void);
 
 #ifdef __cplusplus

@@ -242,3 +242,16 @@ def test_grouped_arbitrary_scales_promote(bs):
         Cr, T = oracle.gemm(gp.A_group(i).numpy(), gp.sA[i].numpy(), gp.B[i].numpy(),
                             gp.sB[i].numpy(), gp.Ms[i], gp.N, gp.K)
         check(bf16_to_f64(outs[i]), Cr, T, f"group{i}")
+
+
+def test_grouped_prebuilt_descriptors_same_bits(bs):
+    gp = workloads.grouped(seed=3, G=4, N=160, K=224, Ms=[9, 64, 1, 30])
+    outs, groups = _grouped_run(bs, gp)
+    again = [torch.empty_like(o) for o in outs]
+    descs = bs.group_descs([(a, sa, b, sb, c) for (a, sa, b, sb, _), c in zip(groups, again)])
+    Ms = torch.tensor(gp.Ms, dtype=torch.int32, device=DEV)
+    for _ in range(2):   # the same descriptor array serves repeated calls
+        bs.fp8_gemm_grouped(descs, Ms, gp.N, gp.K)
+    torch.cuda.synchronize()
+    for g in range(gp.G):
+        assert torch.equal(again[g].view(torch.int16), outs[g].view(torch.int16)), f"group {g}"
