@@ -67,6 +67,8 @@ def _load():
         lib.oracle_gemm_sampled.argtypes = [u8p, fp, u8p, fp, i64, i64, i64,
                                             dp, dp, i64, dp, dp, ctypes.c_int]
         lib.oracle_gemm_sampled.restype = ctypes.c_int
+        lib.oracle_quantize_blocks.argtypes = [dp, i64, i64, u8p, fp]
+        lib.oracle_quantize_blocks.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -167,3 +169,17 @@ def grouped(A_list, sA_list, B_list, sB_list, Ms, N: int, K: int, nthreads: int 
     for A, sA, B, sB, M in zip(A_list, sA_list, B_list, sB_list, Ms):
         out.append(gemm(A, sA, B, sB, int(M), N, K, nthreads))
     return out
+
+
+def quantize_blocks(x_bf16_bits, M: int, K: int):
+    """Block quantization of bf16 activations (x given as its uint16 bit
+    patterns, [M, K]): returns (codes uint8 [M, K], scales float32
+    [ceil(M/32), K/32]) with s = amax/448 per 32x32 block (1 for an all-zero
+    block) and q = E4M3(x/s), fp32 division, nearest-even, saturating."""
+    x = np.ascontiguousarray(np.asarray(x_bf16_bits, dtype=np.uint16).reshape(M, K))
+    q = np.empty((M, K), dtype=np.uint8)
+    s = np.empty(((M + 31) // 32, K // 32), dtype=np.float32)
+    rc = _load().oracle_quantize_blocks(_ptr(x), M, K, _ptr(q), _ptr(s))
+    if rc != 0:
+        raise ValueError("oracle_quantize_blocks: bad arguments")
+    return q, s

@@ -246,3 +246,49 @@ int oracle_gemm_sampled(const uint8_t *A, const float *sA, const uint8_t *B, con
     p.ms = ms; p.ns = ns; p.count = count; p.C = C; p.T = T;
     return run(p, count, nthreads);
 }
+
+/* ------------------------------------------------- block quantization ---- */
+
+/* Activation quantization to the operand format above (FP8 GEMM library
+ * article, hncyxsy.com/news/241433, section 2.1: E4M3 with largest value 448;
+ * section 2.2: one scale per 32x32 block).  For each 32x32 block of the bf16
+ * matrix x [M, K] (row-major; the last row block may be partial):
+ *
+ *   s = amax / 448, an fp32 division (s = 1 when the block is all zero),
+ *   q = E4M3(x / s), the division in fp32, then nearest-even and saturating
+ *       through the search above.
+ *
+ * The quotient is an fp32 value, so the code decision is taken in fp32 as the
+ * stated recipe reads; the search then sees it exactly (fp32 -> fp64 is exact).
+ * q is [M, K] codes, s is [ceil(M/32), K/32] fp32, both row-major.
+ * Returns 0, or -1 on a bad argument. */
+static float bf16_bits_to_float(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+int oracle_quantize_blocks(const uint16_t *x, int64_t M, int64_t K, uint8_t *q, float *s) {
+    if (M < 0 || K < 0 || (K % 32) != 0) return -1;
+    const int64_t MB = (M + 31) / 32, KB = K / 32;
+    for (int64_t mb = 0; mb < MB; ++mb) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            const int64_t r1 = (mb * 32 + 32 < M) ? mb * 32 + 32 : M;
+            float amax = 0.0f;
+            for (int64_t r = mb * 32; r < r1; ++r)
+                for (int64_t c = kb * 32; c < kb * 32 + 32; ++c) {
+                    const float a = fabsf(bf16_bits_to_float(x[r * K + c]));
+                    if (a > amax) amax = a;
+                }
+            const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            s[mb * KB + kb] = sc;
+            for (int64_t r = mb * 32; r < r1; ++r)
+                for (int64_t c = kb * 32; c < kb * 32 + 32; ++c) {
+                    const float t = bf16_bits_to_float(x[r * K + c]) / sc;
+                    q[r * K + c] = (uint8_t)oracle_e4m3_quantize_one((double)t);
+                }
+        }
+    }
+    return 0;
+}

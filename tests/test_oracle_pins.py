@@ -353,3 +353,72 @@ def test_grouped_workload_layout():
     for g in range(4):
         assert gp.sA[g].shape == ((gp.Ms[g] + 31) // 32, 4)
         assert gp.B[g].shape == (64, 128) and gp.sB[g].shape == (2, 4)
+
+
+# ------------------------------------------------------- block quantization
+
+def _bf16_matrix(M, K, seed, outlier_frac=0.005):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(M, K, generator=g)
+    hit = torch.rand(M, K, generator=g) < outlier_frac
+    x = torch.where(hit, x * 50.0, x)
+    x[:, :32] *= 1e-4                                   # tiny values: subnormal codes
+    if M >= 64 and K >= 64:
+        x[32:64, 32:64] = 0.0                           # an all-zero block
+    return x.to(torch.bfloat16)
+
+
+def _bits(xb):
+    return xb.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_quantize_matches_library_cast():
+    """Pinned to torch's float8_e4m3fn cast (round to nearest-even) of the same
+    fp32 quotient, clamped to +-448 first (saturation), with the scale
+    amax/448 computed by torch in fp32."""
+    M, K = 77, 160
+    xb = _bf16_matrix(M, K, seed=11)
+    q, s = oracle.quantize_blocks(_bits(xb), M, K)
+    xf = xb.float()
+    Mp = (M + 31) // 32 * 32
+    pad = torch.zeros(Mp, K)
+    pad[:M] = xf
+    amax = pad.view(Mp // 32, 32, K // 32, 32).abs().amax(dim=(1, 3))
+    s_ref = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    full = s_ref.repeat_interleave(32, 0).repeat_interleave(32, 1)[:M]
+    q_ref = (xf / full).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(s, s_ref.numpy())
+    assert np.array_equal(q, q_ref)
+
+
+def test_quantize_block_maximum_maps_to_448_and_zero_blocks():
+    M, K = 96, 96
+    xb = _bf16_matrix(M, K, seed=12)
+    q, s = oracle.quantize_blocks(_bits(xb), M, K)
+    xf = xb.float().numpy()
+    for mb in range(3):
+        for kb in range(3):
+            blk = xf[32 * mb:32 * mb + 32, 32 * kb:32 * kb + 32]
+            qb = q[32 * mb:32 * mb + 32, 32 * kb:32 * kb + 32]
+            if not blk.any():
+                assert s[mb, kb] == 1.0 and not (qb & 0x7F).any()
+                continue
+            i = np.unravel_index(np.argmax(np.abs(blk)), blk.shape)
+            assert qb[i] == (0xFE if blk[i] < 0 else 0x7E)
+            assert s[mb, kb] == np.float32(np.abs(blk).max()) / np.float32(448.0)
+
+
+def test_quantize_power_of_two_rescaling():
+    """x * 2^j (exact in bf16) gives the same codes and, for blocks that are
+    not all zero (their scale stays 1), scales * 2^j."""
+    M, K = 64, 64
+    xb = _bf16_matrix(M, K, seed=13, outlier_frac=0.0)
+    q0, s0 = oracle.quantize_blocks(_bits(xb), M, K)
+    zero = ~xb.float().view(2, 32, 2, 32).abs().amax(dim=(1, 3)).bool().numpy()
+    assert zero.any() and not zero.all()
+    for j in (-3, 5):
+        xj = (xb.float() * 2.0 ** j).to(torch.bfloat16)
+        assert torch.equal(xj.float(), xb.float() * 2.0 ** j)
+        qj, sj = oracle.quantize_blocks(_bits(xj), M, K)
+        assert np.array_equal(qj, q0)
+        assert np.array_equal(sj, np.where(zero, np.float32(1.0), s0 * np.float32(2.0 ** j)))
