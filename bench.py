@@ -7,8 +7,10 @@ power-of-two 32x32 scales, bf16 out) with inputs resident in HBM; the L2 is
 flushed (a 512 MiB write) between timed steps and each step is timed with CUDA
 events on the launching stream.  The same JSON line also carries the other
 workloads measured the same way: the 8192x28672x8192 prefill projection, the
-grouped decode batch (G=16, M_g in [1,64], N=4096, K=7168; GB/s against HBM)
-and the 8192^3 arbitrary-scale GEMM with outliers (promotion path).
+grouped decode batch (G=16, M_g in [1,64], N=4096, K=7168; GB/s against HBM;
+also as a CUDA-graph replay), the 8192^3 arbitrary-scale GEMM with outliers
+(promotion path) and the block quantization of 8192x8192 bf16 activations
+(GB/s against HBM).
 
 ``--impl reference`` times the CPU oracle (the only other implementation of
 the method; plain C, fp64) on a bounded sample of the same workload.
@@ -43,6 +45,7 @@ WORKLOAD_NAMES = {
     "c2": "prefill projection GEMM M=8192 N=28672 K=8192, pow2 32x32 scales",
     "c3": "grouped decode G=16 M_g~U[1,64] N=4096 K=7168, per-group B, pow2 scales",
     "c4": "arbitrary-scale GEMM M=N=K=8192 (amax/448 scales, 0.5% x50 outliers)",
+    "q8": "block quantization of bf16 activations 8192x8192 -> E4M3 codes + 32x32 fp32 scales",
 }
 
 
@@ -171,6 +174,18 @@ def make_runner(name, dev, bs):
     import torch
 
     import workloads
+    if name == "q8":
+        M = K = 8192
+        g = torch.Generator(device=dev).manual_seed(0)
+        x = torch.randn(M, K, generator=g, device=dev)
+        x = torch.where(torch.rand(M, K, generator=g, device=dev) < 0.005, x * 50.0, x).to(torch.bfloat16)
+        q = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        sc = torch.empty(M // 32, K // 32, dtype=torch.float32, device=dev)
+        nbytes = 2 * M * K + M * K + 4 * sc.numel()
+
+        def run(stream):
+            bs.fp8_quantize_blocks(x, q, sc, stream=stream)
+        return run, 0, nbytes
     p = workloads.make(name, seed=0, device=dev)
     if name == "c3":
         Cs = [torch.empty(m, p.N, dtype=torch.bfloat16, device=dev) for m in p.Ms]
@@ -343,7 +358,7 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     results = {}
-    names = [HEADLINE] + ([] if args.headline_only else ["c2", "c3", "c4"])
+    names = [HEADLINE] + ([] if args.headline_only else ["c2", "c3", "c4", "q8"])
     if args.only:
         names = [args.only]
     with ClockSampler(local) as clk:
@@ -376,7 +391,7 @@ def run_ours(args):
 
     def roofline(name):
         r = results[name]
-        if name == "c3":
+        if name in ("c3", "q8"):
             ach = r["bytes"] / (r["ms"] * 1e-3) / 1e9
             return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
                     "frac": round(ach / hbm_peak, 4), "traffic": recorded_traffic(name),
@@ -392,11 +407,11 @@ def run_ours(args):
         r = results[name]
         entry = {"workload": WORKLOAD_NAMES[name], "ms_per_step": round(r["ms"], 4),
                  "roofline": roofline(name)}
-        if name == "c3":
+        if name in ("c3", "q8"):
             entry["value"] = round(r["bytes"] / (r["ms"] * 1e-3) / 1e9, 1)
             entry["unit"] = "GB/s"
             entry["algorithmic_bytes"] = r["bytes"]
-            if graph_c3:
+            if name == "c3" and graph_c3:
                 entry["graph_replay"] = graph_c3
         else:
             entry["value"] = round(r["flops"] / (r["ms"] * 1e-3) / 1e12, 1)
@@ -491,7 +506,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-elements", type=int, default=65536)
-    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4"], default=None,
+    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "q8"], default=None,
                     help="time one workload only (no e2e, no CPU baseline): profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:

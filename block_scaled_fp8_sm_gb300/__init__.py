@@ -16,6 +16,7 @@ from ._abi import (FP8_PATH_AUTO, FP8_PATH_NATIVE, FP8_PATH_PROMOTE,  # noqa: F4
                    FP8_MAX_GROUPS_PER_LAUNCH, fp8_group_desc)
 
 __all__ = ["fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_gemm_grouped", "group_descs",
+           "fp8_quantize_blocks",
            "fp8_status_query", "fp8_strerror", "fp8_version", "fp8_debug_set", "fp8_lib_shutdown",
            "Fp8Error", "library"]
 
@@ -79,6 +80,22 @@ def fp8_gemm_blockscaled_noalloc(A, sA, B, sB, C, M=None, N=None, K=None, stream
                                                 M, N, K, _stream(stream))
     _check(rc, "fp8_gemm_blockscaled_noalloc")
     return C
+
+
+def fp8_quantize_blocks(x, q=None, s=None, stream=None):
+    """Block quantization of bf16 activations x [M, K] (CUDA tensor) into E4M3
+    codes q [M, K] (uint8) and fp32 scales s [ceil(M/32), K/32]: the A and sA
+    operands of fp8_gemm_blockscaled.  Returns (q, s); allocates them when not
+    given."""
+    import torch
+    M, K = x.shape
+    if q is None:
+        q = torch.empty(M, K, dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty((M + 31) // 32, K // 32, dtype=torch.float32, device=x.device)
+    _check(library().fp8_quantize_blocks(_ptr(x), _ptr(q), _ptr(s), M, K, _stream(stream)),
+           "fp8_quantize_blocks")
+    return q, s
 
 
 class GroupDescs:

@@ -12,6 +12,7 @@
 
 #include "bsfp8.h"
 #include "gemm_kernel.cuh"
+#include "quant_kernel.cuh"
 
 namespace bsfp8 {
 namespace {
@@ -577,6 +578,20 @@ int fp8_debug_set(int key, int64_t value) {
         default:
             return FP8_ERR_MODE;
     }
+}
+
+int fp8_quantize_blocks(const void *x, void *q, float *s, int64_t M, int64_t K, cudaStream_t stream) {
+    const int64_t lim = int64_t(1) << 31;
+    if (M < 0 || K < 0 || M >= lim || K >= lim || (K % 32) != 0) return FP8_ERR_SHAPE;
+    if (M == 0 || K == 0) return FP8_OK;
+    if (!x || !q || !s) return FP8_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(s, 4)) return FP8_ERR_ALIGN;
+    const int64_t MB = (M + 31) / 32;
+    const dim3 grid(static_cast<unsigned>((K + QT_COLS - 1) / QT_COLS),
+                    static_cast<unsigned>(MB < 65535 ? MB : 65535));
+    bsfp8_quantize_blocks<<<grid, QT_THREADS, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x),
+                                                          static_cast<uint8_t *>(q), s, M, K);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
 void fp8_lib_shutdown(void) {

@@ -88,6 +88,22 @@ int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const
                             void *C, int64_t M, int64_t N, int64_t K, int mode,
                             cudaStream_t stream);
 
+/* Block quantization of activations to the operand format above (FP8 GEMM
+ * library article, hncyxsy.com/news/241433, section 2.1: E4M3, largest value
+ * 448; section 2.2: one scale per 32x32 block).  For each 32x32 block of x:
+ *   s = amax / 448 (fp32 division; s = 1 when the block is all zero),
+ *   q = E4M3(x / s) (fp32 division, round to nearest even, saturating at +-448).
+ * x: bf16 [M, K] row-major (16-byte aligned), read only.
+ * q: E4M3 codes [M, K] row-major (16-byte aligned), fully overwritten.
+ * s: fp32 [ceil(M/32), K/32] row-major (4-byte aligned), fully overwritten;
+ *    the last row block may be partial (rows past M do not exist).
+ * q and s are the A and sA operands of fp8_gemm_blockscaled.  K must be a
+ * multiple of 32; M = 0 or K = 0 is a no-op.  NaN or infinite inputs give
+ * undefined codes.  Asynchronous on `stream`; all buffers caller-owned device
+ * memory.  Returns FP8_OK or FP8_ERR_SHAPE / FP8_ERR_NULL / FP8_ERR_ALIGN /
+ * FP8_ERR_CUDA (launch failure). */
+int fp8_quantize_blocks(const void *x, void *q, float *s, int64_t M, int64_t K, cudaStream_t stream);
+
 /* Allocation-free variant of fp8_gemm_blockscaled (AUTO path, same layouts,
  * constraints and results).  The pages have no counterpart: this entry point
  * exists for callers that cannot allocate device memory: an inference server

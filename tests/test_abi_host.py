@@ -79,6 +79,19 @@ def test_null_and_alignment_errors(lib):
     assert lib.fp8_gemm_grouped(arr, 0, 64, 64, 2, None) == _abi.FP8_ERR_NULL
 
 
+def test_quantize_argument_errors(lib):
+    q = lib.fp8_quantize_blocks
+    assert q(16, 16, 16, 64, 48, None) == _abi.FP8_ERR_SHAPE       # K not a multiple of 32
+    assert q(16, 16, 16, -1, 64, None) == _abi.FP8_ERR_SHAPE
+    assert q(16, 16, 16, 1 << 31, 64, None) == _abi.FP8_ERR_SHAPE
+    assert q(0, 0, 0, 0, 64, None) == _abi.FP8_OK                   # empty: nothing enqueued
+    assert q(0, 16, 16, 64, 64, None) == _abi.FP8_ERR_NULL
+    assert q(16, 16, 0, 64, 64, None) == _abi.FP8_ERR_NULL
+    assert q(24, 16, 16, 64, 64, None) == _abi.FP8_ERR_ALIGN
+    assert q(16, 8, 16, 64, 64, None) == _abi.FP8_ERR_ALIGN
+    assert q(16, 16, 18, 64, 64, None) == _abi.FP8_ERR_ALIGN
+
+
 def test_debug_keys(lib):
     assert lib.fp8_debug_set(1, 12345) == _abi.FP8_OK
     assert lib.fp8_debug_set(1, 0) == _abi.FP8_OK
