@@ -687,13 +687,19 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     int s = ot % S, f = ot % FS;
                     uint32_t ph = static_cast<uint32_t>(ot / S) & 1u, phf = static_cast<uint32_t>(ot / FS) & 1u;
                     trace_event(c, TR_MMA_LOOP, i);
+                    // the next stage's barriers are tested (without blocking) just
+                    // before a stage's last MMA, whose issue waits for the pipe anyway
+                    bool next_ready = false;
                     for (int w = 0; w < KW && ok; ++w) {
-                        ok = wait_spin(&ctl->sfready[f], phf, ctl, c);
-                        trace_event(c, TR_MMA_SF_OK, ot + w);
-                        ok = ok && wait_spin(&ctl->full[s], ph, ctl, c);
-                        trace_event(c, TR_MMA_FULL_OK, ot + w);
-                        ok = ok && (!PAIR || wait_spin(&ctl->pfwd[s], ph, ctl, c));
-                        if (!ok) break;
+                        if (!next_ready) {
+                            ok = wait_spin(&ctl->sfready[f], phf, ctl, c);
+                            trace_event(c, TR_MMA_SF_OK, ot + w);
+                            ok = ok && wait_spin(&ctl->full[s], ph, ctl, c);
+                            trace_event(c, TR_MMA_FULL_OK, ot + w);
+                            ok = ok && (!PAIR || wait_spin(&ctl->pfwd[s], ph, ctl, c));
+                            if (!ok) break;
+                        }
+                        next_ready = false;
                         trace_event(c, TR_MMA_READY, ot + w);
                         if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
                         tc_fence_after();
@@ -716,11 +722,21 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         for (int hh = 0; hh < C::HALVES; ++hh) {
 #pragma unroll
                             for (int j = 0; j < KB_PER_STAGE; ++j) {
-                                if (hh * KB_PER_STAGE + j < nk)
+                                if (hh * KB_PER_STAGE + j < nk) {
+                                    if (hh == C::HALVES - 1 && j == KB_PER_STAGE - 1 && w + 1 < KW) {
+                                        const int s2 = s + 1 == S ? 0 : s + 1;
+                                        const int f2 = f + 1 == FS ? 0 : f + 1;
+                                        const uint32_t ph2 = s + 1 == S ? ph ^ 1u : ph;
+                                        const uint32_t phf2 = f + 1 == FS ? phf ^ 1u : phf;
+                                        next_ready = mbar_test_wait(&ctl->sfready[f2], phf2) &&
+                                                     mbar_test_wait(&ctl->full[s2], ph2) &&
+                                                     (!PAIR || mbar_test_wait(&ctl->pfwd[s2], ph2));
+                                    }
                                     mma_block<PAIR>(tmem, ad + static_cast<uint64_t>((hh * C::A_HALF >> 4) + 2 * j),
                                                     bd + static_cast<uint64_t>((hh * C::B_HALF >> 4) + 2 * j),
                                                     idesc_mxf8f6f4(C::TILE_M, BN, j, j), sfa + hh * C::SF_COLS,
                                                     sfa + hh * C::SF_COLS + 4, (w | hh | j) != 0 ? 1u : 0u);
+                                }
                             }
                         }
                         commit_to<PAIR>(&ctl->empty[s]);
