@@ -57,7 +57,7 @@ int set_kernel_attrs() {
                              smem_bytes<BN>()) != cudaSuccess)
         return FP8_ERR_CUDA;
     if (cudaFuncSetAttribute(bsfp8_gemm_grouped<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes<BN>()) != cudaSuccess)
+                             smem_bytes<BN, false, true>()) != cudaSuccess)
         return FP8_ERR_CUDA;
     if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN, true>()) != cudaSuccess)
@@ -332,7 +332,7 @@ int launch_grouped(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, i
         args->e[g].sB = groups[g].sB;
         args->e[g].C = static_cast<__nv_bfloat16 *>(groups[g].C);
     }
-    bsfp8_gemm_grouped<BN><<<d->sm_count, NUM_THREADS, smem_bytes<BN>(), stream>>>(*args);
+    bsfp8_gemm_grouped<BN><<<d->sm_count, NUM_THREADS, smem_bytes<BN, false, true>(), stream>>>(*args);
     delete args;
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }

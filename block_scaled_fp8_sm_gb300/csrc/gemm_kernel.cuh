@@ -73,11 +73,17 @@ constexpr int TILE_N = 256;        // the BN every launch uses
 enum : uint32_t { STATUS_TIMEOUT = 1u, STATUS_SCALE = 2u };
 enum : int { PATH_AUTO = 0, PATH_NATIVE = 1, PATH_PROMOTE = 2 };
 
-template <int BN_, bool PAIR_ = false>
+template <int BN_, bool PAIR_ = false, bool GROUPED_ = false>
 struct Cfg {
     static constexpr int BN = BN_;
     static constexpr bool PAIR = PAIR_;   // CTA pair (cta_group::2): 256-row tiles, B split by columns
-    static constexpr int TILE_M = PAIR ? 2 * BM : BM;               // output rows per tile
+    // Grouped (decode) tiles are 64 rows high: the A slots hold 64 rows, which
+    // leaves room for a fifth operand stage (more weight bytes in flight).  The
+    // M=128 MMA then also reads the 64 rows of shared memory after the slot;
+    // those accumulator rows are never stored.
+    static constexpr bool GROUPED = GROUPED_;
+    static constexpr int TILE_M = PAIR ? 2 * BM : (GROUPED ? BM / 2 : BM);   // output rows per tile
+    static constexpr int MMA_M = PAIR ? 2 * BM : BM;                // rows of every MMA instruction
     // Wide operand stages (CTA pairs) hold two 128-K halves ([half][rows][128
     // B], each a 128-byte-swizzled K-major slice) that arrive as one 3D TMA box
     // per operand: under load the TMA unit's per-request cost dominates, so
@@ -86,8 +92,8 @@ struct Cfg {
     // thread pay their barrier round trips once per 256 K.
     static constexpr bool WIDE = PAIR;
     static constexpr int HALVES = WIDE ? 2 : 1;
-    static constexpr int STAGES = PAIR ? 3 : ((BN == 256) ? 4 : 6);
-    static constexpr int A_HALF = BM * BK;                          // this CTA's A rows, one 128-K half
+    static constexpr int STAGES = PAIR ? 3 : (GROUPED ? 5 : ((BN == 256) ? 4 : 6));
+    static constexpr int A_HALF = (GROUPED ? BM / 2 : BM) * BK;     // this CTA's A rows, one 128-K half
     static constexpr int B_HALF = (PAIR ? BN / 2 : BN) * BK;        // this CTA's B rows, one 128-K half
     static constexpr int A_BYTES = HALVES * A_HALF;                 // per operand stage
     static constexpr int B_BYTES = HALVES * B_HALF;
@@ -209,9 +215,9 @@ struct Tile {
     int m0, n0, Mg, g;
 };
 
-template <int BN, bool PAIR = false>
+template <int BN, bool PAIR = false, bool GROUPED = false>
 constexpr int smem_bytes() {
-    using C = Cfg<BN, PAIR>;
+    using C = Cfg<BN, PAIR, GROUPED>;
     return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES) + C::STG_BYTES +
            C::SF_STAGES * (C::SF_ENTRY + 4 * C::SC_ENTRY) + 2 * 4 * C::PS_FLOATS +
            static_cast<int>(sizeof(Ctrl<C::STAGES, C::SF_STAGES>));
@@ -328,9 +334,9 @@ struct Sched {
             }
             const int g = lo;
             const int Mg = mg[g];
-            const int mtg = (Mg + BM - 1) / BM;
+            const int mtg = (Mg + TILE_M - 1) / TILE_M;
             const int local = t - tile_start[g];
-            r.m0 = (local % mtg) * BM;
+            r.m0 = (local % mtg) * TILE_M;
             r.n0 = (local / mtg) * BN;
             r.Mg = Mg;
             r.g = g;
@@ -442,7 +448,7 @@ __device__ __forceinline__ void commit_to(uint64_t *bar) {
 // ---------------------------------------------------------------------------
 template <int BN, bool GROUPED, bool PAIR, typename Args>
 __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
-    using C = Cfg<BN, PAIR>;
+    using C = Cfg<BN, PAIR, GROUPED>;
     static_assert(!(PAIR && GROUPED), "CTA pairs are used for single problems only");
     constexpr int S = C::STAGES;
     constexpr int NBB = C::NBB;
@@ -516,7 +522,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     m = m < 0 ? 0 : m;
                     ctl->mg[g] = m;
                     ctl->tile_start[g] = acc;
-                    acc += ((m + BM - 1) / BM) * c.nt;
+                    acc += ((m + C::TILE_M - 1) / C::TILE_M) * c.nt;
                 }
                 ctl->tile_start[c.G] = acc;
                 ctl->num_tiles = acc;
@@ -584,7 +590,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             const CUtensorMap *tmb;
             if constexpr (GROUPED) tmb = &args.tmB[tt.g];
             else tmb = &args.tmB;
-            const int a_rows = min(BM, tt.Mg - tt.m0);   // grouped: A rows loaded by cp.async
+            const int a_rows = min(C::TILE_M, tt.Mg - tt.m0);   // grouped: A rows loaded by cp.async
             const uint8_t *a_base = e.A + static_cast<int64_t>(tt.m0) * c.K;
             for (int ks = 0, k0 = 0; ks < KW; ++ks, k0 += C::HALVES * BK) {
                 ok = __all_sync(FULL, wait_bar(&ctl->empty[s], ph ^ 1u, ctl, c));
@@ -734,7 +740,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                                     }
                                     mma_block<PAIR>(tmem, ad + static_cast<uint64_t>((hh * C::A_HALF >> 4) + 2 * j),
                                                     bd + static_cast<uint64_t>((hh * C::B_HALF >> 4) + 2 * j),
-                                                    idesc_mxf8f6f4(C::TILE_M, BN, j, j), sfa + hh * C::SF_COLS,
+                                                    idesc_mxf8f6f4(C::MMA_M, BN, j, j), sfa + hh * C::SF_COLS,
                                                     sfa + hh * C::SF_COLS + 4, (w | hh | j) != 0 ? 1u : 0u);
                                 }
                             }
@@ -807,7 +813,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                                 tc_fence_after();
                                 if constexpr (PAIR) {
                                     mma_f8_pair(tmem + b * BN, ad + static_cast<uint64_t>(2 * j),
-                                                bd + static_cast<uint64_t>(2 * j), idesc_f8f6f4(C::TILE_M, BN), 0u);
+                                                bd + static_cast<uint64_t>(2 * j), idesc_f8f6f4(C::MMA_M, BN), 0u);
                                     mma_commit_pair(&ctl->tfull[b], PAIR_MASK);
                                 } else {
                                     mma_f8(tmem + b * BN, ad + static_cast<uint64_t>(2 * j),
@@ -1027,7 +1033,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             const Tile tt = sch.tile(unit + i * nunits);
             const GroupEntry e = sch.entry(tt.g);
             const int row = tt.m0 + row_off + 32 * q + lane;
-            const bool row_ok = row < tt.Mg;
+            // (grouped tiles own only the first TILE_M of the MMA's 128 rows)
+            const bool row_ok = row < tt.Mg && 32 * q + lane < C::TILE_M;
             const int col0 = h * C::EPI_COLS;
             __nv_bfloat16 *crow = e.C + static_cast<int64_t>(row_ok ? row : 0) * c.N + tt.n0;
 
