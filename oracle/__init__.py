@@ -67,6 +67,8 @@ def _load():
         lib.oracle_gemm_sampled.argtypes = [u8p, fp, u8p, fp, i64, i64, i64,
                                             dp, dp, i64, dp, dp, ctypes.c_int]
         lib.oracle_gemm_sampled.restype = ctypes.c_int
+        lib.oracle_gemm_rowcol.argtypes = [u8p, fp, u8p, fp, i64, i64, i64, dp, dp]
+        lib.oracle_gemm_rowcol.restype = ctypes.c_int
         lib.oracle_quantize_blocks.argtypes = [dp, i64, i64, u8p, fp]
         lib.oracle_quantize_blocks.restype = ctypes.c_int
         _lib = lib
@@ -183,3 +185,18 @@ def quantize_blocks(x_bf16_bits, M: int, K: int):
     if rc != 0:
         raise ValueError("oracle_quantize_blocks: bad arguments")
     return q, s
+
+
+def gemm_rowcol(A, sA, B, sB, M: int, N: int, K: int):
+    """Per-token x per-channel scaled GEMM: C[m,n] = sA[m]*sB[n]*sum_k A*B with
+    sA [M] and sB [N] fp32 (per-tensor: constant vectors).  Returns (C, T) in
+    fp64, like gemm()."""
+    A = _codes(A, M, K)
+    B = _codes(B, N, K)
+    sA = np.ascontiguousarray(np.asarray(sA, dtype=np.float32).reshape(M))
+    sB = np.ascontiguousarray(np.asarray(sB, dtype=np.float32).reshape(N))
+    C = np.empty((M, N), dtype=np.float64)
+    T = np.empty((M, N), dtype=np.float64)
+    if _load().oracle_gemm_rowcol(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), M, N, K, _ptr(C), _ptr(T)) != 0:
+        raise ValueError("oracle_gemm_rowcol: bad arguments")
+    return C, T

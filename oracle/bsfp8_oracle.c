@@ -292,3 +292,35 @@ int oracle_quantize_blocks(const uint16_t *x, int64_t M, int64_t K, uint8_t *q, 
     }
     return 0;
 }
+
+/* ------------------------------------------ per-token x per-channel ---- */
+
+/* Scales that do not vary along K (FP8 GEMM library article, section 2.2:
+ * per-tensor, per-channel and per-token granularities; section 2.3: such
+ * scales are applied in the GEMM's epilogue):
+ *
+ *   C[m,n] = sA[m] * sB[n] * sum_k A[m,k] * B[n,k]
+ *
+ * with sA [M] (per token / row of A) and sB [N] (per output channel / row of
+ * B) fp32; a per-tensor scale is the constant vector.  The K sum is EXACT in
+ * fp64 for K <= 2^15: each product is a multiple of 2^-18 below 2^18, so the
+ * sum needs at most 51 bits.  It is then multiplied once by sA*sB (exact in
+ * fp64).  T = |sA*sB| * sum_k |A*B|.  Returns 0, or -1 on a bad argument. */
+int oracle_gemm_rowcol(const uint8_t *A, const float *sA, const uint8_t *B, const float *sB,
+                       int64_t M, int64_t N, int64_t K, double *C, double *T) {
+    if (M < 0 || N < 0 || K < 0 || K > (int64_t)1 << 15) return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double p = e4m3_value(A[m * K + k]) * e4m3_value(B[n * K + k]);
+                acc += p;
+                mag += fabs(p);
+            }
+            const double s = (double)sA[m] * (double)sB[n];
+            C[m * N + n] = s * acc;
+            T[m * N + n] = fabs(s) * mag;
+        }
+    }
+    return 0;
+}

@@ -422,3 +422,70 @@ def test_quantize_power_of_two_rescaling():
         qj, sj = oracle.quantize_blocks(_bits(xj), M, K)
         assert np.array_equal(qj, q0)
         assert np.array_equal(sj, np.where(zero, np.float32(1.0), s0 * np.float32(2.0 ** j)))
+
+
+# ------------------------------------------------ per-token x per-channel
+
+def test_rowcol_per_tensor_closed_form():
+    """Constant vectors (a per-tensor scale): alpha*beta times numpy's fp64
+    matmul of the decoded operands, exact here (partial sums are multiples of
+    2^-18 below 2^35)."""
+    M, N, K = 45, 64, 320
+    A, _, B, _ = _rand_problem(M, N, K, seed=21)
+    tab = oracle.e4m3_table()
+    alpha, beta = np.float32(0.3), np.float32(1.7)
+    C, T = oracle.gemm_rowcol(A, np.full(M, alpha), B, np.full(N, beta), M, N, K)
+    prod = tab[A] @ tab[B].T
+    assert np.array_equal(C, (float(alpha) * float(beta)) * prod)
+    assert np.array_equal(T, (float(alpha) * float(beta)) * (np.abs(tab[A]) @ np.abs(tab[B]).T))
+
+
+def test_rowcol_identity_and_one_hot():
+    """B = identity gives C[m,n] = sA[m]*sB[n]*A[m,n]; a one-hot A row picks
+    one column of B."""
+    M, K = 40, 64
+    N = K
+    rng = np.random.default_rng(22)
+    A, _, _, _ = _rand_problem(M, N, K, seed=22)
+    B = np.zeros((N, K), dtype=np.uint8)
+    B[np.arange(N), np.arange(K)] = 0x38                        # 1.0
+    sA = (rng.random(M) * 4 - 2).astype(np.float32)              # includes negative scales
+    sB = (rng.random(N) * 3).astype(np.float32)
+    tab = oracle.e4m3_table()
+    C, _ = oracle.gemm_rowcol(A, sA, B, sB, M, N, K)
+    assert np.array_equal(C, (sA.astype(np.float64)[:, None] * sB.astype(np.float64)[None, :]) * tab[A])
+    A1 = np.zeros((M, K), dtype=np.uint8)
+    ks = rng.integers(0, K, M)
+    A1[np.arange(M), ks] = 0x40                                  # 2.0
+    _, _, B2, _ = _rand_problem(M, 96, K, seed=23)
+    sB2 = (rng.random(96) + 0.5).astype(np.float32)
+    C1, _ = oracle.gemm_rowcol(A1, sA, B2, sB2, M, 96, K)
+    for m in range(M):
+        exp = (float(sA[m]) * sB2.astype(np.float64)) * 2.0 * tab[B2[:, ks[m]]]
+        assert np.array_equal(C1[m], exp)
+
+
+def test_rowcol_agrees_with_block_oracle_on_block_constant_scales():
+    """Scales constant over 32-row and 32-column blocks are also 32x32 block
+    scales: the separately pinned block-scaled oracle must agree within its
+    fp64 rounding (one rounding per K block there, none here)."""
+    M, N, K = 64, 96, 256
+    A, _, B, _ = _rand_problem(M, N, K, seed=24)
+    rng = np.random.default_rng(24)
+    a = (rng.random(M // 32) * 2 + 0.1).astype(np.float32)
+    b = (rng.random(N // 32) * 2 + 0.1).astype(np.float32)
+    Cr, Tr = oracle.gemm_rowcol(A, np.repeat(a, 32), B, np.repeat(b, 32), M, N, K)
+    Cb, Tb = oracle.gemm(A, np.repeat(a[:, None], K // 32, axis=1), B, np.repeat(b[:, None], K // 32, axis=1), M, N, K)
+    assert np.all(np.abs(Cr - Cb) <= 1e-12 * Tr)
+    assert np.allclose(Tr, Tb, rtol=1e-12, atol=0)
+
+
+def test_rowcol_operand_swap_symmetry():
+    M, N, K = 33, 64, 96
+    A, _, B, _ = _rand_problem(M, N, K, seed=25)
+    rng = np.random.default_rng(25)
+    sA = rng.random(M).astype(np.float32)
+    sB = rng.random(N).astype(np.float32)
+    C, _ = oracle.gemm_rowcol(A, sA, B, sB, M, N, K)
+    Ct, _ = oracle.gemm_rowcol(B, sB, A, sA, N, M, K)
+    assert np.array_equal(C, Ct.T)
