@@ -9,8 +9,8 @@ events on the launching stream.  The same JSON line also carries the other
 workloads measured the same way: the 8192x28672x8192 prefill projection, the
 grouped decode batch (G=16, M_g in [1,64], N=4096, K=7168; GB/s against HBM;
 also as a CUDA-graph replay), the 8192^3 arbitrary-scale GEMM with outliers
-(promotion path) and the block quantization of 8192x8192 bf16 activations
-(GB/s against HBM).
+(promotion path), the block quantization of 8192x8192 bf16 activations
+(GB/s against HBM) and the 4096^3 GEMM with per-token x per-channel scales.
 
 ``--impl reference`` times the CPU oracle (the only other implementation of
 the method; plain C, fp64) on a bounded sample of the same workload.
@@ -46,6 +46,7 @@ WORKLOAD_NAMES = {
     "c3": "grouped decode G=16 M_g~U[1,64] N=4096 K=7168, per-group B, pow2 scales",
     "c4": "arbitrary-scale GEMM M=N=K=8192 (amax/448 scales, 0.5% x50 outliers)",
     "q8": "block quantization of bf16 activations 8192x8192 -> E4M3 codes + 32x32 fp32 scales",
+    "r1": "per-token x per-channel scaled E4M3 GEMM M=N=K=4096 (fp32 scales [M] and [N]), bf16 out",
 }
 
 
@@ -186,6 +187,17 @@ def make_runner(name, dev, bs):
         def run(stream):
             bs.fp8_quantize_blocks(x, q, sc, stream=stream)
         return run, 0, nbytes
+    if name == "r1":
+        p = workloads.make("c1", seed=0, device=dev)
+        g = torch.Generator(device=dev).manual_seed(1)
+        sA = torch.rand(p.M, generator=g, device=dev) + 0.5
+        sB = torch.rand(p.N, generator=g, device=dev) + 0.5
+        C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
+        nbytes = p.M * p.K + p.N * p.K + 4 * (p.M + p.N) + 2 * p.M * p.N
+
+        def run(stream):
+            bs.fp8_gemm_rowcol(p.A, sA, p.B, sB, C, p.M, p.N, p.K, stream=stream)
+        return run, p.flops, nbytes
     p = workloads.make(name, seed=0, device=dev)
     if name == "c3":
         Cs = [torch.empty(m, p.N, dtype=torch.bfloat16, device=dev) for m in p.Ms]
@@ -358,7 +370,7 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     results = {}
-    names = [HEADLINE] + ([] if args.headline_only else ["c2", "c3", "c4", "q8"])
+    names = [HEADLINE] + ([] if args.headline_only else ["c2", "c3", "c4", "q8", "r1"])
     if args.only:
         names = [args.only]
     with ClockSampler(local) as clk:
@@ -506,7 +518,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-elements", type=int, default=65536)
-    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "q8"], default=None,
+    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "q8", "r1"], default=None,
                     help="time one workload only (no e2e, no CPU baseline): profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -285,10 +285,12 @@ int launch_plain(const void *A, const float *sA, const void *B, const float *sB,
 // 128 of B's 256 columns; the grid is a whole number of pairs.
 template <int BN>
 int launch_pair(const void *A, const float *sA, const void *B, const float *sB, void *C,
-                int64_t M, int64_t N, int64_t K, int mode, DeviceState *d, cudaStream_t stream) {
+                int64_t M, int64_t N, int64_t K, int mode, DeviceState *d, cudaStream_t stream,
+                int scale_kind = SCALE_BLOCK32) {
     PlainArgs args;
     std::memset(&args, 0, sizeof args);
     fill_common(args.c, M, N, K, mode, d, BN);
+    args.c.scale_kind = scale_kind;
     args.c.mt = static_cast<int>((M + 2 * BM - 1) / (2 * BM));
     args.c.num_tiles = args.c.mt * args.c.nt;
     int rc = encode_kmajor(&args.tmA, A, M, K, BM);
@@ -473,6 +475,25 @@ int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const
 int fp8_gemm_blockscaled(const void *A, const float *sA, const void *B, const float *sB, void *C,
                          int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     return fp8_gemm_blockscaled_ex(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, stream);
+}
+
+int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                    int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != FP8_OK) return rc;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!C) return FP8_ERR_NULL;
+    if (!aligned(C, 16)) return FP8_ERR_ALIGN;
+    if (K > 0) {
+        if (!A || !B || !sA || !sB) return FP8_ERR_NULL;
+        if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 4) || !aligned(sB, 4))
+            return FP8_ERR_ALIGN;
+    }
+    DeviceState *d = nullptr;
+    rc = device_setup(&d);
+    if (rc != FP8_OK) return rc;
+    if (K == 0) return zero_fill(C, M * N, stream);
+    return launch_pair<TILE_N>(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, d, stream, SCALE_ROWCOL);
 }
 
 int fp8_gemm_blockscaled_noalloc(const void *A, const float *sA, const void *B, const float *sB,

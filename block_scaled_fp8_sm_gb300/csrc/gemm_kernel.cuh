@@ -72,6 +72,10 @@ constexpr int TILE_N = 256;        // the BN every launch uses
 
 enum : uint32_t { STATUS_TIMEOUT = 1u, STATUS_SCALE = 2u };
 enum : int { PATH_AUTO = 0, PATH_NATIVE = 1, PATH_PROMOTE = 2 };
+// SCALE_BLOCK32: sA [ceil(M/32)][K/32], sB [N/32][K/32] block scales.
+// SCALE_ROWCOL: sA [M] and sB [N], constant along K: the MMAs run with unit
+// scales and the epilogue multiplies each output by sA[m] * sB[n].
+enum : int { SCALE_BLOCK32 = 0, SCALE_ROWCOL = 1 };
 
 template <int BN_, bool PAIR_ = false, bool GROUPED_ = false>
 struct Cfg {
@@ -131,6 +135,7 @@ struct Common {
     int M, N, K, KB, KS;     // KB = K/32, KS = stages per tile
     int mt, nt, num_tiles;   // plain problem tiling
     int mode;
+    int scale_kind;          // SCALE_BLOCK32 or SCALE_ROWCOL
     int G;
     const int32_t *Ms;       // grouped: device row counts
     uint32_t *status;
@@ -565,7 +570,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     if (warp != 0 && warp != 3) {
         constexpr int SCANNERS = NUM_THREADS - 64;
         bool bad = false;
-        if (my_tiles > 0 && c.mode != PATH_PROMOTE) {
+        if (my_tiles > 0 && c.mode != PATH_PROMOTE && c.scale_kind == SCALE_BLOCK32) {
             const Tile tt = sch.tile(unit);
             const int t = static_cast<int>(threadIdx.x) - (warp < 3 ? 32 : 64);
             bad = tile_has_bad_scale<BN, C::TILE_M>(tt, sch.entry(tt.g), c, t, SCANNERS);
@@ -856,7 +861,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             int verdict = 1;
-            if (c.mode != PATH_PROMOTE) {
+            if (c.scale_kind == SCALE_ROWCOL) {
+                verdict = 0;   // unit block scales: the native path
+            } else if (c.mode != PATH_PROMOTE) {
                 bool any_bad;
                 if (i == 0) {
                     any_bad = ctl->first_bad != 0;   // computed by warps 1..11 at the start
@@ -924,8 +931,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 #pragma unroll
                     for (int h = 0; h < H; ++h) {
                         const float *sc = sm_sc + bs * C::SC_ENTRY + h * C::SC_FLOATS;
-                        const float va = lane < 16 ? sc[lane] : 1.0f;
-                        const float vb = lane < 4 * NBB ? sc[16 + lane] : 1.0f;
+                        // (per-row / per-column scales: unit lines, 2^0)
+                        const float va = (lane < 16 && c.scale_kind == SCALE_BLOCK32) ? sc[lane] : 1.0f;
+                        const float vb = (lane < 4 * NBB && c.scale_kind == SCALE_BLOCK32) ? sc[16 + lane] : 1.0f;
                         wa[h] = ue8m0_of(va) << (8 * (lane & 3));
                         wb[h] = ue8m0_of(vb) << (8 * (lane & 3));
                     }
@@ -988,17 +996,21 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 ok = __all_sync(FULL, wait_bar(&ctl->sfempty[is], iph ^ 1u, ctl, c));
                 if (!ok) break;
                 if (lane == 0) trace_event(c, TR_SCALE_ISSUE, it);
-                const uint32_t sc = smem_u32(sm_sc + is * C::SC_ENTRY);
+                if (c.scale_kind == SCALE_ROWCOL) {
+                    mbar_arrive(&ctl->scfull[is]);   // nothing to stage: unit block scales
+                } else {
+                    const uint32_t sc = smem_u32(sm_sc + is * C::SC_ENTRY);
 #pragma unroll
-                for (int h = 0; h < H; ++h) {
-                    const int kb = (iks * H + h) * KB_PER_STAGE;   // first K block of the half
-                    const bool kb_ok = kb + (lane & 3) < c.KB;
-                    const bool ca = a_in && kb_ok, cb = b_in && kb_ok;
-                    if (lane < 16) cp_async_4(sc + 4 * (h * C::SC_FLOATS + lane), ca ? pa + kb : pa, ca ? 4u : 0u);
-                    if (lane < 4 * NBB)
-                        cp_async_4(sc + 4 * (h * C::SC_FLOATS + 16 + lane), cb ? pb + kb : pb, cb ? 4u : 0u);
+                    for (int h = 0; h < H; ++h) {
+                        const int kb = (iks * H + h) * KB_PER_STAGE;   // first K block of the half
+                        const bool kb_ok = kb + (lane & 3) < c.KB;
+                        const bool ca = a_in && kb_ok, cb = b_in && kb_ok;
+                        if (lane < 16) cp_async_4(sc + 4 * (h * C::SC_FLOATS + lane), ca ? pa + kb : pa, ca ? 4u : 0u);
+                        if (lane < 4 * NBB)
+                            cp_async_4(sc + 4 * (h * C::SC_FLOATS + 16 + lane), cb ? pb + kb : pb, cb ? 4u : 0u);
+                    }
+                    cp_async_mbar_arrive_noinc(&ctl->scfull[is]);
                 }
-                cp_async_mbar_arrive_noinc(&ctl->scfull[is]);
                 if (++is == FS) { is = 0; iph ^= 1u; }
             }
         }
@@ -1064,8 +1076,16 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     // one TMA store of the 128 x 32 box (rows past M are clipped)
                     __nv_bfloat16 *stg = sm_stg + h * (BM * C::STG_COLS);
                     uint4 *mine = reinterpret_cast<uint4 *>(stg + (32 * q + lane) * C::STG_COLS);
+                    // per-row / per-column scales: this thread's row factor
+                    const float rs = (c.scale_kind == SCALE_ROWCOL && row_ok) ? __ldg(e.sA + row) : 1.0f;
 #pragma unroll
                     for (int x = 0; x < NCH; ++x) {
+                        if (c.scale_kind == SCALE_ROWCOL && tt.n0 + col0 + 32 * x < c.N) {
+                            const float *cs = e.sB + tt.n0 + col0 + 32 * x;   // 32 column factors (broadcast)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                r[x][j] = __float_as_uint(__uint_as_float(r[x][j]) * (rs * __ldg(cs + j)));
+                        }
                         pack_bf16x32(mine, r[x]);
                         fence_proxy_async_smem();
                         named_bar_sync(bar_id, HALF_THREADS);

@@ -88,6 +88,21 @@ int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const
                             void *C, int64_t M, int64_t N, int64_t K, int mode,
                             cudaStream_t stream);
 
+/* GEMM with scales that do not vary along K (FP8 GEMM library article,
+ * hncyxsy.com/news/241433, section 2.2: per-tensor, per-channel and per-token
+ * scale granularities; section 2.3: such scales are applied in the GEMM's
+ * epilogue):
+ *   C[m,n] = bf16( sA[m] * sB[n] * sum_k A[m,k] * B[n,k] )
+ * A, B, C, M, N, K: as fp8_gemm_blockscaled.  sA: fp32 [M] (per token / row
+ * of A), sB: fp32 [N] (per output channel / row of B), 4-byte aligned, read
+ * only; a per-tensor scale is a constant vector.  The MMAs run with unit
+ * scales and accumulate over all of K in fp32; the epilogue multiplies by
+ * sA[m] * sB[n] (one fp32 product) and rounds to bf16 (nearest even).  Same
+ * tiles and K order as the block-scaled call, so rows are batch-invariant.
+ * Returns FP8_OK or FP8_ERR_SHAPE / FP8_ERR_NULL / FP8_ERR_ALIGN / FP8_ERR_CUDA. */
+int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                    int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* Block quantization of activations to the operand format above (FP8 GEMM
  * library article, hncyxsy.com/news/241433, section 2.1: E4M3, largest value
  * 448; section 2.2: one scale per 32x32 block).  For each 32x32 block of x:
