@@ -10,7 +10,8 @@ workloads measured the same way: the 8192x28672x8192 prefill projection, the
 grouped decode batch (G=16, M_g in [1,64], N=4096, K=7168; GB/s against HBM;
 also as a CUDA-graph replay), the 8192^3 arbitrary-scale GEMM with outliers
 (promotion path), the block quantization of 8192x8192 bf16 activations
-(GB/s against HBM) and the 4096^3 GEMM with per-token x per-channel scales.
+(GB/s against HBM), the 4096^3 GEMM with per-token x per-channel scales and
+the 4096^3 GEMM with a fused residual add.
 
 ``--impl reference`` times the CPU oracle (the only other implementation of
 the method; plain C, fp64) on a bounded sample of the same workload.
@@ -47,6 +48,7 @@ WORKLOAD_NAMES = {
     "c4": "arbitrary-scale GEMM M=N=K=8192 (amax/448 scales, 0.5% x50 outliers)",
     "q8": "block quantization of bf16 activations 8192x8192 -> E4M3 codes + 32x32 fp32 scales",
     "r1": "per-token x per-channel scaled E4M3 GEMM M=N=K=4096 (fp32 scales [M] and [N]), bf16 out",
+    "f1": "block-scaled E4M3 GEMM M=N=K=4096 with a bf16 residual added in the epilogue",
 }
 
 
@@ -187,6 +189,14 @@ def make_runner(name, dev, bs):
         def run(stream):
             bs.fp8_quantize_blocks(x, q, sc, stream=stream)
         return run, 0, nbytes
+    if name == "f1":
+        p = workloads.make("c1", seed=0, device=dev)
+        R = torch.randn(p.M, p.N, device=dev).to(torch.bfloat16)
+        C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
+
+        def run(stream):
+            bs.fp8_gemm_blockscaled_residual(p.A, p.sA, p.B, p.sB, R, C, p.M, p.N, p.K, stream=stream)
+        return run, p.flops, p.algorithmic_bytes + 2 * p.M * p.N
     if name == "r1":
         p = workloads.make("c1", seed=0, device=dev)
         g = torch.Generator(device=dev).manual_seed(1)
@@ -370,7 +380,7 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     results = {}
-    names = [HEADLINE] + ([] if args.headline_only else ["c2", "c3", "c4", "q8", "r1"])
+    names = [HEADLINE] + ([] if args.headline_only else ["c2", "c3", "c4", "q8", "r1", "f1"])
     if args.only:
         names = [args.only]
     with ClockSampler(local) as clk:
@@ -518,7 +528,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-elements", type=int, default=65536)
-    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "q8", "r1"], default=None,
+    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "q8", "r1", "f1"], default=None,
                     help="time one workload only (no e2e, no CPU baseline): profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:

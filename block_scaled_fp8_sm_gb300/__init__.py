@@ -16,7 +16,7 @@ from ._abi import (FP8_PATH_AUTO, FP8_PATH_NATIVE, FP8_PATH_PROMOTE,  # noqa: F4
                    FP8_MAX_GROUPS_PER_LAUNCH, fp8_group_desc)
 
 __all__ = ["fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_gemm_grouped", "group_descs",
-           "fp8_quantize_blocks", "fp8_gemm_rowcol",
+           "fp8_quantize_blocks", "fp8_gemm_rowcol", "fp8_gemm_blockscaled_residual",
            "fp8_status_query", "fp8_strerror", "fp8_version", "fp8_debug_set", "fp8_lib_shutdown",
            "Fp8Error", "library"]
 
@@ -79,6 +79,17 @@ def fp8_gemm_blockscaled_noalloc(A, sA, B, sB, C, M=None, N=None, K=None, stream
     rc = library().fp8_gemm_blockscaled_noalloc(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C),
                                                 M, N, K, _stream(stream))
     _check(rc, "fp8_gemm_blockscaled_noalloc")
+    return C
+
+
+def fp8_gemm_blockscaled_residual(A, sA, B, sB, R, C, M=None, N=None, K=None, stream=None):
+    """C = bf16(block-scaled GEMM + R): the residual R (bf16 [M, N], may be C
+    itself) added in fp32 in the epilogue before the one bf16 rounding."""
+    M = A.shape[0] if M is None else M
+    K = A.shape[1] if K is None else K
+    N = B.shape[0] if N is None else N
+    _check(library().fp8_gemm_blockscaled_residual(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(R), _ptr(C),
+                                                   M, N, K, _stream(stream)), "fp8_gemm_blockscaled_residual")
     return C
 
 

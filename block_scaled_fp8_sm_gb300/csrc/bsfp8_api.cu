@@ -286,7 +286,7 @@ int launch_plain(const void *A, const float *sA, const void *B, const float *sB,
 template <int BN>
 int launch_pair(const void *A, const float *sA, const void *B, const float *sB, void *C,
                 int64_t M, int64_t N, int64_t K, int mode, DeviceState *d, cudaStream_t stream,
-                int scale_kind = SCALE_BLOCK32) {
+                int scale_kind = SCALE_BLOCK32, const void *R = nullptr) {
     PlainArgs args;
     std::memset(&args, 0, sizeof args);
     fill_common(args.c, M, N, K, mode, d, BN);
@@ -307,6 +307,11 @@ int launch_pair(const void *A, const float *sA, const void *B, const float *sB, 
     args.e.sA = sA;
     args.e.sB = sB;
     args.e.C = static_cast<__nv_bfloat16 *>(C);
+    if (R != nullptr) {
+        args.e.R = static_cast<const __nv_bfloat16 *>(R);
+        rc = encode_out(&args.tmR, const_cast<void *>(R), M, N);
+        if (rc != FP8_OK) return rc;
+    }
     const int pairs = args.c.num_tiles < d->sm_count / 2 ? args.c.num_tiles : d->sm_count / 2;
     bsfp8_gemm_pair<BN><<<2 * pairs, NUM_THREADS, smem_bytes<BN, true>(), stream>>>(args);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
@@ -475,6 +480,32 @@ int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const
 int fp8_gemm_blockscaled(const void *A, const float *sA, const void *B, const float *sB, void *C,
                          int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     return fp8_gemm_blockscaled_ex(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, stream);
+}
+
+int fp8_gemm_blockscaled_residual(const void *A, const float *sA, const void *B, const float *sB,
+                                  const void *R, void *C, int64_t M, int64_t N, int64_t K,
+                                  cudaStream_t stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != FP8_OK) return rc;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!C || !R) return FP8_ERR_NULL;
+    if (!aligned(C, 16) || !aligned(R, 16)) return FP8_ERR_ALIGN;
+    if (K > 0) {
+        if (!A || !B || !sA || !sB) return FP8_ERR_NULL;
+        if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 4) || !aligned(sB, 4))
+            return FP8_ERR_ALIGN;
+    }
+    DeviceState *d = nullptr;
+    rc = device_setup(&d);
+    if (rc != FP8_OK) return rc;
+    if (K == 0) {   // C = R
+        if (C == R) return FP8_OK;
+        return cudaMemcpyAsync(C, R, static_cast<size_t>(M * N) * 2, cudaMemcpyDeviceToDevice, stream) ==
+                       cudaSuccess
+                   ? FP8_OK
+                   : FP8_ERR_CUDA;
+    }
+    return launch_pair<TILE_N>(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, d, stream, SCALE_BLOCK32, R);
 }
 
 int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *sB, void *C,

@@ -129,6 +129,7 @@ struct GroupEntry {
     const float *sA;
     const float *sB;
     __nv_bfloat16 *C;
+    const __nv_bfloat16 *R;   // single problems: optional residual added to C (nullptr: none)
 };
 
 struct Common {
@@ -181,6 +182,7 @@ struct PlainArgs {
     CUtensorMap tmA;
     CUtensorMap tmB;
     CUtensorMap tmC;    // bf16 output {N, M}, box {32, 128}: epilogue TMA stores
+    CUtensorMap tmR;    // bf16 residual, same shape and box (when e.R is set)
     CUtensorMap tmA3;   // wide stages: {128 K bytes, rows, K/128 halves} views of A and B
     CUtensorMap tmB3;
     GroupEntry e;
@@ -207,6 +209,7 @@ struct Ctrl {
     uint64_t vfull[2];          // verdict -> MMA, scale and epilogue warps
     uint64_t vempty[2];
     uint64_t drain;
+    uint64_t rfull[2];          // residual chunk of column half h landed in its staging buffer
     uint32_t tmem_base;
     int verdict[2];
     int first_bad;              // the CTA's first tile reads a non-power-of-two scale
@@ -417,6 +420,21 @@ __device__ __forceinline__ void pack_bf16x32(uint4 *dst, const uint32_t *r) {
     }
 }
 
+// r[j] (fp32 bits) += the 32 bf16 values in 64 bytes of shared memory.
+__device__ __forceinline__ void add_bf16x32(uint32_t *r, const uint4 *src) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint4 u = src[w];
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            r[8 * w + 2 * k] = __float_as_uint(__uint_as_float(r[8 * w + 2 * k]) + __uint_as_float(wv[k] << 16));
+            r[8 * w + 2 * k + 1] =
+                __float_as_uint(__uint_as_float(r[8 * w + 2 * k + 1]) + __uint_as_float(wv[k] & 0xFFFF0000u));
+        }
+    }
+}
+
 __device__ __forceinline__ void store_bf16x32f(__nv_bfloat16 *dst, const float *v) {
     uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
@@ -504,6 +522,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             mbar_init(&ctl->vempty[b], 2 + NUM_EPI_WARPS);   // MMA + scale warp + epilogue
         }
         mbar_init(&ctl->drain, 1);
+        mbar_init(&ctl->rfull[0], 1);
+        mbar_init(&ctl->rfull[1], 1);
         ctl->abort = 0;
         ctl->first_bad = 0;
         fence_mbar_init();
@@ -1035,6 +1055,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         const uint32_t bar_id = 1u + static_cast<uint32_t>(h);
         constexpr uint32_t HALF_THREADS = 128;
         const bool issuer = q == 0 && lane == 0;
+        uint32_t rph = 0;             // residual chunks loaded for this column half (rfull phase)
+        bool r_pending = false;       // issuer: a residual load may still be landing
         for (int i = 0; i < my_tiles; ++i) {
             const int v = i & 1;
             bool ok = wait_bar(&ctl->vfull[v], static_cast<uint32_t>(i >> 1) & 1u, ctl, c);
@@ -1086,6 +1108,31 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                             for (int j = 0; j < 32; ++j)
                                 r[x][j] = __float_as_uint(__uint_as_float(r[x][j]) * (rs * __ldg(cs + j)));
                         }
+                        if constexpr (!GROUPED) {
+                            if (e.R != nullptr) {
+                                // the residual chunk comes into the staging buffer by TMA
+                                // first (rows past M read as zero); each thread adds its row
+                                const int col = tt.n0 + col0 + 32 * x;
+                                if (issuer) {
+                                    if (col < c.N) {
+                                        mbar_arrive_expect_tx(&ctl->rfull[h], BM * C::STG_COLS * 2);
+                                        tma_load_2d(&args.tmR, &ctl->rfull[h], stg, col, tt.m0 + row_off);
+                                        r_pending = true;
+                                    } else {
+                                        mbar_arrive(&ctl->rfull[h]);   // keeps the phase sequence
+                                    }
+                                }
+                                bool rok = __all_sync(FULL, wait_bar(&ctl->rfull[h], rph & 1u, ctl, c));
+                                rok = named_bar_and(bar_id, HALF_THREADS, rok);   // the half leaves together
+                                ++rph;
+                                if (!rok) {
+                                    ok = false;
+                                    break;
+                                }
+                                if (issuer) r_pending = false;
+                                add_bf16x32(r[x], mine);
+                            }
+                        }
                         pack_bf16x32(mine, r[x]);
                         fence_proxy_async_smem();
                         named_bar_sync(bar_id, HALF_THREADS);
@@ -1099,6 +1146,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         }
                         named_bar_sync(bar_id, HALF_THREADS);   // the buffer is free again
                     }
+                    if (!ok) break;
                 } else if (row_ok) {
 #pragma unroll
                     for (int x = 0; x < NCH; ++x)
@@ -1147,14 +1195,37 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 if (!ok) break;
                 if (row_ok) {
 #pragma unroll
-                    for (int x = 0; x < NCH; ++x)
-                        if (tt.n0 + col0 + 32 * x < c.N) store_bf16x32f(crow + col0 + 32 * x, acc + 32 * x);
+                    for (int x = 0; x < NCH; ++x) {
+                        if (tt.n0 + col0 + 32 * x >= c.N) continue;
+                        if constexpr (!GROUPED) {
+                            if (e.R != nullptr) {   // residual of this row (16-byte loads)
+                                const uint4 *rr = reinterpret_cast<const uint4 *>(
+                                    e.R + static_cast<int64_t>(row) * c.N + tt.n0 + col0 + 32 * x);
+#pragma unroll
+                                for (int w = 0; w < 4; ++w) {
+                                    const uint4 u = __ldg(rr + w);
+                                    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                                    for (int k = 0; k < 4; ++k) {
+                                        acc[32 * x + 8 * w + 2 * k] += __uint_as_float(wv[k] << 16);
+                                        acc[32 * x + 8 * w + 2 * k + 1] += __uint_as_float(wv[k] & 0xFFFF0000u);
+                                    }
+                                }
+                            }
+                        }
+                        store_bf16x32f(crow + col0 + 32 * x, acc + 32 * x);
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->vempty[v]);
         }
-        if (TMA_OUT && issuer) bulk_wait_all();   // the output is written before the CTA exits
+        if (TMA_OUT && issuer) {
+            // no residual load may still be landing, and the output is written,
+            // before the CTA exits
+            if (r_pending) wait_bar_drain(&ctl->rfull[h], (rph - 1u) & 1u, c.wait_limit);
+            bulk_wait_all();
+        }
     }
 
     tc_fence_before();

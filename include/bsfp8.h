@@ -88,6 +88,20 @@ int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const
                             void *C, int64_t M, int64_t N, int64_t K, int mode,
                             cudaStream_t stream);
 
+/* Block-scaled GEMM with a residual added in the epilogue (FP8 GEMM library
+ * article, hncyxsy.com/news/241433, section 2.3 and the pitfalls of section 5:
+ * element-wise work fused into the GEMM's tail instead of another pass over
+ * the output):
+ *   C[m,n] = bf16( sum_kb sA*sB*sum_k A*B  +  R[m,n] )
+ * The accumulator and R (bf16, exact in fp32) are added in fp32 and rounded
+ * once to bf16 (nearest even).  R: bf16 [M, N] row-major, 16-byte aligned,
+ * read only; it may be the same buffer as C (in place).  Everything else as
+ * fp8_gemm_blockscaled (AUTO path); K = 0 gives C = R.
+ * Returns FP8_OK or FP8_ERR_SHAPE / FP8_ERR_NULL / FP8_ERR_ALIGN / FP8_ERR_CUDA. */
+int fp8_gemm_blockscaled_residual(const void *A, const float *sA, const void *B, const float *sB,
+                                  const void *R, void *C, int64_t M, int64_t N, int64_t K,
+                                  cudaStream_t stream);
+
 /* GEMM with scales that do not vary along K (FP8 GEMM library article,
  * hncyxsy.com/news/241433, section 2.2: per-tensor, per-channel and per-token
  * scale granularities; section 2.3: such scales are applied in the GEMM's

@@ -102,6 +102,15 @@ def test_rowcol_argument_errors(lib):
     assert r(16, 18, 16, 16, 16, 64, 64, 64, None) == _abi.FP8_ERR_ALIGN
 
 
+def test_residual_argument_errors(lib):
+    r = lib.fp8_gemm_blockscaled_residual
+    assert r(16, 16, 16, 16, 16, 16, 64, 33, 64, None) == _abi.FP8_ERR_SHAPE
+    assert r(0, 0, 0, 0, 0, 0, 0, 64, 64, None) == _abi.FP8_OK          # M == 0: nothing enqueued
+    assert r(16, 16, 16, 16, 0, 16, 64, 64, 64, None) == _abi.FP8_ERR_NULL
+    assert r(16, 16, 16, 16, 8, 16, 64, 64, 64, None) == _abi.FP8_ERR_ALIGN
+    assert r(16, 16, 16, 16, 16, 8, 64, 64, 64, None) == _abi.FP8_ERR_ALIGN
+
+
 def test_debug_keys(lib):
     assert lib.fp8_debug_set(1, 12345) == _abi.FP8_OK
     assert lib.fp8_debug_set(1, 0) == _abi.FP8_OK
