@@ -62,6 +62,12 @@ int set_kernel_attrs() {
     if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN, true>()) != cudaSuccess)
         return FP8_ERR_CUDA;
+    if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN, SCALE_ROWCOL, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<BN, true>()) != cudaSuccess)
+        return FP8_ERR_CUDA;
+    if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN, SCALE_BLOCK32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<BN, true>()) != cudaSuccess)
+        return FP8_ERR_CUDA;
     return FP8_OK;
 }
 
@@ -283,14 +289,13 @@ int launch_plain(const void *A, const float *sA, const void *B, const float *sB,
 
 // CTA-pair launch: 256-row tiles, each CTA of a pair loads 128 rows of A and
 // 128 of B's 256 columns; the grid is a whole number of pairs.
-template <int BN>
+template <int BN, int SK = SCALE_BLOCK32, bool RES = false>
 int launch_pair(const void *A, const float *sA, const void *B, const float *sB, void *C,
                 int64_t M, int64_t N, int64_t K, int mode, DeviceState *d, cudaStream_t stream,
-                int scale_kind = SCALE_BLOCK32, const void *R = nullptr) {
+                const void *R = nullptr) {
     PlainArgs args;
     std::memset(&args, 0, sizeof args);
     fill_common(args.c, M, N, K, mode, d, BN);
-    args.c.scale_kind = scale_kind;
     args.c.mt = static_cast<int>((M + 2 * BM - 1) / (2 * BM));
     args.c.num_tiles = args.c.mt * args.c.nt;
     int rc = encode_kmajor(&args.tmA, A, M, K, BM);
@@ -307,13 +312,13 @@ int launch_pair(const void *A, const float *sA, const void *B, const float *sB, 
     args.e.sA = sA;
     args.e.sB = sB;
     args.e.C = static_cast<__nv_bfloat16 *>(C);
-    if (R != nullptr) {
-        args.e.R = static_cast<const __nv_bfloat16 *>(R);
+    if constexpr (RES) {
+        args.R = static_cast<const __nv_bfloat16 *>(R);
         rc = encode_out(&args.tmR, const_cast<void *>(R), M, N);
         if (rc != FP8_OK) return rc;
     }
     const int pairs = args.c.num_tiles < d->sm_count / 2 ? args.c.num_tiles : d->sm_count / 2;
-    bsfp8_gemm_pair<BN><<<2 * pairs, NUM_THREADS, smem_bytes<BN, true>(), stream>>>(args);
+    bsfp8_gemm_pair<BN, SK, RES><<<2 * pairs, NUM_THREADS, smem_bytes<BN, true>(), stream>>>(args);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -505,7 +510,7 @@ int fp8_gemm_blockscaled_residual(const void *A, const float *sA, const void *B,
                    ? FP8_OK
                    : FP8_ERR_CUDA;
     }
-    return launch_pair<TILE_N>(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, d, stream, SCALE_BLOCK32, R);
+    return launch_pair<TILE_N, SCALE_BLOCK32, true>(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, d, stream, R);
 }
 
 int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *sB, void *C,
@@ -524,7 +529,7 @@ int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *
     rc = device_setup(&d);
     if (rc != FP8_OK) return rc;
     if (K == 0) return zero_fill(C, M * N, stream);
-    return launch_pair<TILE_N>(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, d, stream, SCALE_ROWCOL);
+    return launch_pair<TILE_N, SCALE_ROWCOL, false>(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, d, stream);
 }
 
 int fp8_gemm_blockscaled_noalloc(const void *A, const float *sA, const void *B, const float *sB,

@@ -72,6 +72,8 @@ constexpr int TILE_N = 256;        // the BN every launch uses
 
 enum : uint32_t { STATUS_TIMEOUT = 1u, STATUS_SCALE = 2u };
 enum : int { PATH_AUTO = 0, PATH_NATIVE = 1, PATH_PROMOTE = 2 };
+// Scale layouts (a kernel template parameter, so each layout compiles its own
+// kernel and the block-scaled kernels carry no code for the others):
 // SCALE_BLOCK32: sA [ceil(M/32)][K/32], sB [N/32][K/32] block scales.
 // SCALE_ROWCOL: sA [M] and sB [N], constant along K: the MMAs run with unit
 // scales and the epilogue multiplies each output by sA[m] * sB[n].
@@ -129,14 +131,12 @@ struct GroupEntry {
     const float *sA;
     const float *sB;
     __nv_bfloat16 *C;
-    const __nv_bfloat16 *R;   // single problems: optional residual added to C (nullptr: none)
 };
 
 struct Common {
     int M, N, K, KB, KS;     // KB = K/32, KS = stages per tile
     int mt, nt, num_tiles;   // plain problem tiling
     int mode;
-    int scale_kind;          // SCALE_BLOCK32 or SCALE_ROWCOL
     int G;
     const int32_t *Ms;       // grouped: device row counts
     uint32_t *status;
@@ -182,11 +182,12 @@ struct PlainArgs {
     CUtensorMap tmA;
     CUtensorMap tmB;
     CUtensorMap tmC;    // bf16 output {N, M}, box {32, 128}: epilogue TMA stores
-    CUtensorMap tmR;    // bf16 residual, same shape and box (when e.R is set)
     CUtensorMap tmA3;   // wide stages: {128 K bytes, rows, K/128 halves} views of A and B
     CUtensorMap tmB3;
     GroupEntry e;
     Common c;
+    CUtensorMap tmR;    // residual kernels: bf16 residual, same shape and box as C
+    const __nv_bfloat16 *R;
 };
 
 struct GroupedArgs {
@@ -469,7 +470,8 @@ __device__ __forceinline__ void commit_to(uint64_t *bar) {
 }
 
 // ---------------------------------------------------------------------------
-template <int BN, bool GROUPED, bool PAIR, typename Args>
+// SK: scale layout; RES: a bf16 residual is added before the bf16 rounding.
+template <int BN, bool GROUPED, bool PAIR, typename Args, int SK = SCALE_BLOCK32, bool RES = false>
 __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     using C = Cfg<BN, PAIR, GROUPED>;
     static_assert(!(PAIR && GROUPED), "CTA pairs are used for single problems only");
@@ -590,7 +592,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     if (warp != 0 && warp != 3) {
         constexpr int SCANNERS = NUM_THREADS - 64;
         bool bad = false;
-        if (my_tiles > 0 && c.mode != PATH_PROMOTE && c.scale_kind == SCALE_BLOCK32) {
+        if (my_tiles > 0 && c.mode != PATH_PROMOTE && SK == SCALE_BLOCK32) {
             const Tile tt = sch.tile(unit);
             const int t = static_cast<int>(threadIdx.x) - (warp < 3 ? 32 : 64);
             bad = tile_has_bad_scale<BN, C::TILE_M>(tt, sch.entry(tt.g), c, t, SCANNERS);
@@ -881,7 +883,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             ok = __all_sync(FULL, ok);
             if (!ok) break;
             int verdict = 1;
-            if (c.scale_kind == SCALE_ROWCOL) {
+            if constexpr (SK == SCALE_ROWCOL) {
                 verdict = 0;   // unit block scales: the native path
             } else if (c.mode != PATH_PROMOTE) {
                 bool any_bad;
@@ -952,8 +954,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     for (int h = 0; h < H; ++h) {
                         const float *sc = sm_sc + bs * C::SC_ENTRY + h * C::SC_FLOATS;
                         // (per-row / per-column scales: unit lines, 2^0)
-                        const float va = (lane < 16 && c.scale_kind == SCALE_BLOCK32) ? sc[lane] : 1.0f;
-                        const float vb = (lane < 4 * NBB && c.scale_kind == SCALE_BLOCK32) ? sc[16 + lane] : 1.0f;
+                        const float va = (lane < 16 && SK == SCALE_BLOCK32) ? sc[lane] : 1.0f;
+                        const float vb = (lane < 4 * NBB && SK == SCALE_BLOCK32) ? sc[16 + lane] : 1.0f;
                         wa[h] = ue8m0_of(va) << (8 * (lane & 3));
                         wb[h] = ue8m0_of(vb) << (8 * (lane & 3));
                     }
@@ -1016,7 +1018,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 ok = __all_sync(FULL, wait_bar(&ctl->sfempty[is], iph ^ 1u, ctl, c));
                 if (!ok) break;
                 if (lane == 0) trace_event(c, TR_SCALE_ISSUE, it);
-                if (c.scale_kind == SCALE_ROWCOL) {
+                if constexpr (SK == SCALE_ROWCOL) {
                     mbar_arrive(&ctl->scfull[is]);   // nothing to stage: unit block scales
                 } else {
                     const uint32_t sc = smem_u32(sm_sc + is * C::SC_ENTRY);
@@ -1099,17 +1101,17 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     __nv_bfloat16 *stg = sm_stg + h * (BM * C::STG_COLS);
                     uint4 *mine = reinterpret_cast<uint4 *>(stg + (32 * q + lane) * C::STG_COLS);
                     // per-row / per-column scales: this thread's row factor
-                    const float rs = (c.scale_kind == SCALE_ROWCOL && row_ok) ? __ldg(e.sA + row) : 1.0f;
+                    const float rs = (SK == SCALE_ROWCOL && row_ok) ? __ldg(e.sA + row) : 1.0f;
 #pragma unroll
                     for (int x = 0; x < NCH; ++x) {
-                        if (c.scale_kind == SCALE_ROWCOL && tt.n0 + col0 + 32 * x < c.N) {
+                        if (SK == SCALE_ROWCOL && tt.n0 + col0 + 32 * x < c.N) {
                             const float *cs = e.sB + tt.n0 + col0 + 32 * x;   // 32 column factors (broadcast)
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
                                 r[x][j] = __float_as_uint(__uint_as_float(r[x][j]) * (rs * __ldg(cs + j)));
                         }
-                        if constexpr (!GROUPED) {
-                            if (e.R != nullptr) {
+                        if constexpr (RES) {
+                            {
                                 // the residual chunk comes into the staging buffer by TMA
                                 // first (rows past M read as zero); each thread adds its row
                                 const int col = tt.n0 + col0 + 32 * x;
@@ -1197,10 +1199,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 #pragma unroll
                     for (int x = 0; x < NCH; ++x) {
                         if (tt.n0 + col0 + 32 * x >= c.N) continue;
-                        if constexpr (!GROUPED) {
-                            if (e.R != nullptr) {   // residual of this row (16-byte loads)
+                        if constexpr (RES) {
+                            {   // residual of this row (16-byte loads)
                                 const uint4 *rr = reinterpret_cast<const uint4 *>(
-                                    e.R + static_cast<int64_t>(row) * c.N + tt.n0 + col0 + 32 * x);
+                                    args.R + static_cast<int64_t>(row) * c.N + tt.n0 + col0 + 32 * x);
 #pragma unroll
                                 for (int w = 0; w < 4; ++w) {
                                     const uint4 u = __ldg(rr + w);
@@ -1245,11 +1247,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bsfp8_gemm_plain(const __grid_
 }
 
 // CTA-pair variant: clusters of two CTAs, 256-row tiles, pair MMAs.
-template <int BN>
+template <int BN, int SK = SCALE_BLOCK32, bool RES = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     bsfp8_gemm_pair(const __grid_constant__ PlainArgs args) {
     extern __shared__ uint8_t smem_raw[];
-    gemm_body<BN, false, true>(args, smem_raw);
+    gemm_body<BN, false, true, PlainArgs, SK, RES>(args, smem_raw);
 }
 
 template <int BN>
