@@ -7,36 +7,48 @@
 // for one problem or for a group of independent problems (same article,
 // section 4.2: one launch, each block looks up its problem in a table).
 //
-// Output tile: 128 rows x BN (256) columns; one tcgen05.mma is M=128, N=BN,
-// K=32 (one 32-K scale block).  On this part an M=128 MMA costs ~116 cycles for
-// any N <= 128 but only ~140-165 for N = 256, so N = 256 is what reaches the
-// tensor peak.  The MMA issue blocks until the previous MMA retires, so the
-// issuing thread does nothing else.
+// Kernels (one body, gemm_body):
+//   bsfp8_gemm_pair     single problems on CTA pairs (cta_group::2): 256 x 256
+//                       output tiles, one M=256/N=256/K=32 MMA per 32-K block
+//                       issued by the pair's leader; operand stages of 256 K
+//                       arrive as one 3D TMA box per operand; template
+//                       variants for per-row/column scales and a fused
+//                       residual add
+//   bsfp8_gemm_plain    single problems, one CTA per 128 x 256 tile (the
+//                       allocation-free entry point)
+//   bsfp8_gemm_grouped  many decode problems in one launch: 64-row tiles, A
+//                       rows by cp.async (their count lives on the device)
+// An M=128 MMA costs ~116 cycles for any N <= 128 but only ~160 for N = 256,
+// so N = 256 is what reaches the tensor peak.  The MMA issue blocks until the
+// pipe accepts the next MMA (it holds about one), so the issuing thread does
+// as little as possible between MMAs.
 //
-// Roles (384 threads, one CTA per SM, persistent over output tiles):
+// Roles (384 threads, one CTA per SM, persistent over output tiles; in a pair
+// each CTA runs every role on its half and the peer's MMA warp forwards its
+// readiness to the leader with relaxed cluster-scope arrives):
 //   warp 0     producer: TMA loads of the A and B K-slices into a ring of
-//              shared-memory stages (128-byte swizzle; for grouped problems the
-//              A rows come by cp.async since their count lives on the device),
-//              and cp.async of the stage's fp32 block scales.  Only
-//              asynchronous copies: each lane's cp.async completion arrives on
-//              the stage barrier by itself.
-//   warp 1     MMA issuer.  Native path: lane 0 copies the stage's UE8M0 scale
-//              lines into tensor memory (tcgen05.cp) and issues the four
-//              kind::mxf8f6f4 block-scaled MMAs into the accumulator.
-//              Promotion path: the warp publishes the K block's scale products
-//              and lane 0 issues one unscaled kind::f8f6f4 MMA per 32-K block
-//              into one of two tensor-memory partials.
-//   warp 2     path verdict: scans each tile's scales one or two tiles ahead
-//              and decides native (all positive normal powers of two) or
-//              promotion.
-//   warp 3     scale warp: turns each stage's fp32 scales into the 32
-//              identical 16-byte UE8M0 lines per 128 rows that tcgen05.cp
-//              replicates into all lane quarters, then releases the stage to
-//              the MMA warp.
+//              shared-memory stages (128-byte swizzle; grouped problems: A
+//              rows by cp.async).
+//   warp 1     MMA issuer.  Native path: lane 0 copies a stage's UE8M0 scale
+//              lines into tensor memory (tcgen05.cp) and issues its
+//              kind::mxf8f6f4 block-scaled MMAs back to back, testing the next
+//              stage's barriers before the last one.  Promotion path: the warp
+//              publishes each K block's scale products and lane 0 issues one
+//              unscaled kind::f8f6f4 MMA per 32-K block into one of two
+//              tensor-memory partials.
+//   warp 2     path verdict: scans each tile's scales ahead of time and decides
+//              native (all positive normal powers of two) or promotion; the
+//              first tile's scan is shared by warps 1, 2 and 4-11 at start.
+//   warp 3     scale warp: cp.async of each stage's fp32 scales into a ring
+//              that runs ahead of the operand ring, then the UE8M0 lines (8
+//              identical 16-byte lines per 128 rows, read four times by
+//              tcgen05.cp) that the MMA warp copies into tensor memory.
 //   warps 4-11 epilogue: native tiles drain the accumulator into registers,
 //              release it to the MMA warp at once, then convert to bf16 and
-//              store; promotion tiles accumulate acc += (sA*sB) * partial per
-//              32-K block in fp32 registers and store at the end.
+//              write 128 x 32 chunks through a shared-memory staging buffer
+//              with TMA stores (grouped tiles: 16-byte stores); promotion
+//              tiles accumulate acc += (sA*sB) * partial per 32-K block in fp32
+//              registers and store at the end.
 //
 // The K loop of every tile runs whole and in ascending K order, with a tile
 // shape that depends only on the kernel, never on M: no split-K, no stream-K,
