@@ -32,10 +32,12 @@
 //   warp 1     MMA issuer.  Native path: lane 0 copies a stage's UE8M0 scale
 //              lines into tensor memory (tcgen05.cp) and issues its
 //              kind::mxf8f6f4 block-scaled MMAs back to back, testing the next
-//              stage's barriers before the last one.  Promotion path: the warp
-//              publishes each K block's scale products and lane 0 issues one
-//              unscaled kind::f8f6f4 MMA per 32-K block into one of two
-//              tensor-memory partials.
+//              stage's barriers before the last one.  Promotion path: lane 0
+//              issues one unscaled kind::f8f6f4 MMA and one commit per 32-K
+//              block into one of two tensor-memory partials (a commit holds
+//              the tensor pipe for a few hundred cycles, so partials are as
+//              wide as tensor memory allows); the warp releases a stage's
+//              scale entry once the epilogue has read all of its partials.
 //   warp 2     path verdict: scans each tile's scales ahead of time and decides
 //              native (all positive normal powers of two) or promotion; the
 //              first tile's scan is shared by warps 1, 2 and 4-11 at start.
@@ -48,7 +50,8 @@
 //              write 128 x 32 chunks through a shared-memory staging buffer
 //              with TMA stores (grouped tiles: 16-byte stores); promotion
 //              tiles accumulate acc += (sA*sB) * partial per 32-K block in fp32
-//              registers and store at the end.
+//              registers, with sA and sB read from the stage's scale entry,
+//              and store at the end.
 //
 // The K loop of every tile runs whole and in ascending K order, with a tile
 // shape that depends only on the kernel, never on M: no split-K, no stream-K,
@@ -132,10 +135,9 @@ struct Cfg {
     static constexpr int NBB = BN / 32;                             // 32-column blocks per tile
     static constexpr int SC_FLOATS = 16 + 4 * NBB;                  // staged fp32 scales per 128-K half
     static constexpr int SC_ENTRY = HALVES * SC_FLOATS;
-    static constexpr int PS_FLOATS = 4 * NBB;                       // scale products per K block
     static_assert(SF_COL0 + SF_STAGES * SF_ENTRY_COLS <= 512 && SF_COL0 >= BN, "tensor memory budget");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
-    static_assert(4 * NBB <= 32, "one scale product per MMA-warp lane");
+    static_assert(4 * NBB <= 32, "one scale lane per 32-column block");
 };
 
 struct GroupEntry {
@@ -218,7 +220,6 @@ struct Ctrl {
     uint64_t sfempty[SF_STAGES];  // MMA commit -> scale warp (lines and scales consumed)
     uint64_t tfull[2];          // MMA commit -> epilogue (accumulator / partial b)
     uint64_t tempty[2];         // epilogue -> MMA
-    uint64_t pfull[2];          // MMA warp -> epilogue (scale products of partial b)
     uint64_t vfull[2];          // verdict -> MMA, scale and epilogue warps
     uint64_t vempty[2];
     uint64_t drain;
@@ -240,7 +241,7 @@ template <int BN, bool PAIR = false, bool GROUPED = false>
 constexpr int smem_bytes() {
     using C = Cfg<BN, PAIR, GROUPED>;
     return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES) + C::STG_BYTES +
-           C::SF_STAGES * (C::SF_ENTRY + 4 * C::SC_ENTRY) + 2 * 4 * C::PS_FLOATS +
+           C::SF_STAGES * (C::SF_ENTRY + 4 * C::SC_ENTRY) +
            static_cast<int>(sizeof(Ctrl<C::STAGES, C::SF_STAGES>));
 }
 
@@ -500,9 +501,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     uint8_t *sm_sf = sm_b + S * C::B_BYTES + C::STG_BYTES;                   // [FS][HALVES][SF_BYTES]
     constexpr int FS = C::SF_STAGES;
     float *sm_sc = reinterpret_cast<float *>(sm_sf + FS * C::SF_ENTRY);      // [FS][HALVES][SC_FLOATS]
-    float *sm_ps = sm_sc + FS * C::SC_ENTRY;                                   // [2][PS_FLOATS]
     using CtrlT = Ctrl<S, FS>;
-    CtrlT *ctl = reinterpret_cast<CtrlT *>(sm_ps + 2 * C::PS_FLOATS);
+    CtrlT *ctl = reinterpret_cast<CtrlT *>(sm_sc + FS * C::SC_ENTRY);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -531,7 +531,6 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tfull[b], 1);
             mbar_init(&ctl->tempty[b], (PAIR && leader) ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
-            mbar_init(&ctl->pfull[b], 1);
             mbar_init(&ctl->vfull[b], 1);
             mbar_init(&ctl->vempty[b], 2 + NUM_EPI_WARPS);   // MMA + scale warp + epilogue
         }
@@ -706,7 +705,24 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         const int KW = (c.KS + C::HALVES - 1) / C::HALVES;
         uint32_t uses0 = 0, uses1 = 0;    // completed uses of tensor-memory buffers 0 / 1
         uint32_t pk = 0;                  // promotion partials issued (buffer = pk & 1)
-        uint32_t pu0 = 0, pu1 = 0;        // promotion uses of buffers 0 / 1 (pfull phases)
+        // Promotion tiles: the epilogue reads each K block's scales from the
+        // scale ring, so an entry is released (sfempty) only once the epilogue
+        // has read every partial of its stage.  The MMA warp learns that from
+        // its own tempty waits (the wait for partial p passes once partial p-2
+        // has been read); entries wait here, oldest first, with the index of
+        // their last partial.
+        int pend_f0 = -1, pend_l0 = 0, pend_f1 = -1, pend_l1 = 0;
+        auto release_read = [&](int upto) {   // partials <= upto have been read
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                if (pend_f0 >= 0 && pend_l0 <= upto) {
+                    if (lane == 0) mbar_arrive(&ctl->sfempty[pend_f0]);
+                    pend_f0 = pend_f1;
+                    pend_l0 = pend_l1;
+                    pend_f1 = -1;
+                }
+            }
+        };
         bool ok = true;
         bool issued = false;
         for (int i = 0; i < my_tiles && ok; ++i) {
@@ -714,6 +730,14 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             ok = __all_sync(FULL, wait_bar(&ctl->vfull[v], static_cast<uint32_t>(i >> 1) & 1u, ctl, c));
             if (!ok) break;
             const bool promote = ctl->verdict[v] != 0;
+            if (!promote && pend_f0 >= 0) {
+                // a promotion tile's last scale entries: both buffers drained
+                // means every partial has been read
+                ok = __all_sync(FULL, wait_bar(&ctl->tempty[0], (uses0 & 1u) ^ 1u, ctl, c) &&
+                                          wait_bar(&ctl->tempty[1], (uses1 & 1u) ^ 1u, ctl, c));
+                if (!ok) break;
+                release_read(static_cast<int>(pk));
+            }
             if (!promote) {
                 if (lane == 0 && leader) {
                     trace_event(c, TR_MMA_VOK, i);
@@ -831,7 +855,6 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         mbar_signal_cluster(mapa_shared(&ctl->pfwd[s], 0));
                     }
                     if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
-                    const float *sc = sm_sc + f * C::SC_ENTRY + hh * C::SC_FLOATS;
                     const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES + hh * C::A_HALF));
                     const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES + hh * C::B_HALF));
                     const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
@@ -840,14 +863,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         const uint32_t ub = b ? uses1 : uses0;
                         ok = __all_sync(FULL, wait_bar(&ctl->tempty[b], (ub & 1u) ^ 1u, ctl, c));
                         if (!ok) break;
-                        // scale products of this K block: ps[rb*NBB + cb] = sA[rb]*sB[cb]
-                        if (lane < 4 * NBB) {
-                            const int rb = lane / NBB, cb = lane % NBB;
-                            sm_ps[b * C::PS_FLOATS + lane] = sc[rb * 4 + j] * sc[16 + cb * 4 + j];
-                        }
-                        __syncwarp();
+                        release_read(static_cast<int>(pk) - 2);
                         if (lane == 0) {
-                            mbar_arrive(&ctl->pfull[b]);
                             if (leader) {
                                 tc_fence_after();
                                 if constexpr (PAIR) {
@@ -862,15 +879,15 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                             }
                         }
                         issued = true;
-                        if (b) { ++uses1; ++pu1; } else { ++uses0; ++pu0; }
+                        if (b) ++uses1; else ++uses0;
                         ++pk;
                     }
                     if (!ok) break;
-                    if (lane == 0 && leader) {
-                        if (stage_done) {
-                            commit_to<PAIR>(&ctl->empty[s]);
-                            commit_to<PAIR>(&ctl->sfempty[f]);
-                        }
+                    if (stage_done) {
+                        if (lane == 0 && leader) commit_to<PAIR>(&ctl->empty[s]);
+                        // the stage's scale entry, released once its partials are read
+                        if (pend_f0 < 0) { pend_f0 = f; pend_l0 = static_cast<int>(pk) - 1; }
+                        else { pend_f1 = f; pend_l1 = static_cast<int>(pk) - 1; }
                     }
                     __syncwarp();
                 }
@@ -1057,14 +1074,17 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         constexpr int NCH = C::EPI_COLS / 32;         // 32-column chunks per warp
         uint32_t uses0 = 0, uses1 = 0, pk = 0;
-        uint32_t pu0 = 0, pu1 = 0;   // promotion uses of buffers 0 / 1 (pfull phases)
+        int eft = 0;   // scale-ring entries of the tiles before this one
         // Single problems write native tiles through shared memory with TMA
         // stores: one lane per output row would otherwise flood the load/store
         // path with row-scattered stores for thousands of cycles, and the MMA
         // thread's barrier operations queue behind them.  The four warps of a
         // column half share a staging buffer and a named barrier; every exit
         // from the loop is agreed among them first (named_bar_and), so no warp
-        // is ever left waiting at that barrier.
+        // is ever left waiting at that barrier.  A promotion tile agrees once,
+        // after its K loop: a warp whose wait failed skips the rest of the loop
+        // and the others' waits end on the abort flag, so all reach that point
+        // (agreeing per K block would hold the four warps in lockstep).
         constexpr bool TMA_OUT = !GROUPED;
         const uint32_t bar_id = 1u + static_cast<uint32_t>(h);
         constexpr uint32_t HALF_THREADS = 128;
@@ -1169,22 +1189,38 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_STORED, i);
             } else {
                 if (pk & 1u) ++pk;
+                // Each K block's scales come from the stage's scale-ring entry
+                // (the MMA warp releases an entry only after every partial of
+                // its stage has been read here): row block q of this CTA, the
+                // warp's NCH column blocks.
+                int f = eft % FS, hh = 0, j = 0;
+                uint32_t fph = static_cast<uint32_t>(eft / FS) & 1u;
                 float acc[C::EPI_COLS];
 #pragma unroll
                 for (int x = 0; x < C::EPI_COLS; ++x) acc[x] = 0.0f;
                 for (int kb = 0; kb < c.KB; ++kb) {
                     const uint32_t b = pk & 1u;
                     const uint32_t ub = b ? uses1 : uses0;
-                    const uint32_t pb = b ? pu1 : pu0;
-                    ok = wait_bar(&ctl->pfull[b], pb & 1u, ctl, c) &&
-                         wait_bar(&ctl->tfull[b], ub & 1u, ctl, c);
-                    ok = __all_sync(FULL, ok);
-                    if constexpr (TMA_OUT) ok = named_bar_and(bar_id, HALF_THREADS, ok);
-                    if (!ok) break;
-                    tc_fence_after();
+                    if (hh == 0 && j == 0) {   // a new stage: its entry has landed
+                        ok = __all_sync(FULL, wait_bar(&ctl->sfready[f], fph, ctl, c));
+                        if (!ok) break;
+                    }
+                    // scale products sA * sB of this K block, one per 32-column block
+                    const float *se = sm_sc + f * C::SC_ENTRY + hh * C::SC_FLOATS;
+                    const float sa = se[q * 4 + j];
                     float sc[NCH];
 #pragma unroll
-                    for (int x = 0; x < NCH; ++x) sc[x] = sm_ps[b * C::PS_FLOATS + q * NBB + h * NCH + x];
+                    for (int x = 0; x < NCH; ++x) sc[x] = sa * se[16 + (h * NCH + x) * 4 + j];
+                    if (++j == KB_PER_STAGE) {
+                        j = 0;
+                        if (++hh == C::HALVES) {
+                            hh = 0;
+                            if (++f == FS) { f = 0; fph ^= 1u; }
+                        }
+                    }
+                    ok = __all_sync(FULL, wait_bar(&ctl->tfull[b], ub & 1u, ctl, c));
+                    if (!ok) break;
+                    tc_fence_after();
                     const uint32_t pbase = tmem + lane_base + b * BN + col0;
 #pragma unroll
                     for (int x = 0; x < 2 * NCH; ++x) {
@@ -1203,9 +1239,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         for (int y = 0; y < 16; ++y)
                             acc[16 * x + y] = fmaf(sc[x >> 1], __uint_as_float(r[y]), acc[16 * x + y]);
                     }
-                    if (b) { ++uses1; ++pu1; } else { ++uses0; ++pu0; }
+                    if (b) ++uses1; else ++uses0;
                     ++pk;
                 }
+                if constexpr (TMA_OUT) ok = named_bar_and(bar_id, HALF_THREADS, ok);
                 if (!ok) break;
                 if (row_ok) {
 #pragma unroll
@@ -1231,6 +1268,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     }
                 }
             }
+            eft += (c.KS + C::HALVES - 1) / C::HALVES;
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->vempty[v]);
         }
