@@ -937,8 +937,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         // One ring entry per operand stage (HALVES x 128 K).  Loads the
         // entry's fp32 block scales with cp.async -- per half h, lane l < 16:
         // sA[m0/32 + l/4][kb0 + 4h + l%4]; lane l < 4*BN/32: sB[n0/32 + l/4][kb0
-        // + 4h + l%4] -- L entries ahead of turning them into the UE8M0 lines
-        // that tcgen05.cp replicates into all lane quarters.  Absent blocks read
+        // + 4h + l%4], stored K-block-major (sA at [j][row block], sB at 16 +
+        // [j][column block]) -- L entries ahead of turning them into the UE8M0
+        // lines that tcgen05.cp replicates into all lane quarters.  Absent blocks read
         // as zero: they only meet discarded rows or K past the end.  Handling a
         // whole operand stage per pass pays the barrier round trips once per
         // 256 K on wide stages.
@@ -983,8 +984,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     for (int h = 0; h < H; ++h) {
                         const float *sc = sm_sc + bs * C::SC_ENTRY + h * C::SC_FLOATS;
                         // (per-row / per-column scales: unit lines, 2^0)
-                        const float va = (lane < 16 && SK == SCALE_BLOCK32) ? sc[lane] : 1.0f;
-                        const float vb = (lane < 4 * NBB && SK == SCALE_BLOCK32) ? sc[16 + lane] : 1.0f;
+                        const float va = (lane < 16 && SK == SCALE_BLOCK32) ? sc[(lane & 3) * 4 + (lane >> 2)] : 1.0f;
+                        const float vb = (lane < 4 * NBB && SK == SCALE_BLOCK32) ? sc[16 + (lane & 3) * NBB + (lane >> 2)] : 1.0f;
                         wa[h] = ue8m0_of(va) << (8 * (lane & 3));
                         wb[h] = ue8m0_of(vb) << (8 * (lane & 3));
                     }
@@ -1056,9 +1057,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         const int kb = (iks * H + h) * KB_PER_STAGE;   // first K block of the half
                         const bool kb_ok = kb + (lane & 3) < c.KB;
                         const bool ca = a_in && kb_ok, cb = b_in && kb_ok;
-                        if (lane < 16) cp_async_4(sc + 4 * (h * C::SC_FLOATS + lane), ca ? pa + kb : pa, ca ? 4u : 0u);
+                        if (lane < 16) cp_async_4(sc + 4 * (h * C::SC_FLOATS + (lane & 3) * 4 + (lane >> 2)), ca ? pa + kb : pa, ca ? 4u : 0u);
                         if (lane < 4 * NBB)
-                            cp_async_4(sc + 4 * (h * C::SC_FLOATS + 16 + lane), cb ? pb + kb : pb, cb ? 4u : 0u);
+                            cp_async_4(sc + 4 * (h * C::SC_FLOATS + 16 + (lane & 3) * NBB + (lane >> 2)), cb ? pb + kb : pb, cb ? 4u : 0u);
                     }
                     cp_async_mbar_arrive_noinc(&ctl->scfull[is]);
                 }
@@ -1207,10 +1208,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     }
                     // scale products sA * sB of this K block, one per 32-column block
                     const float *se = sm_sc + f * C::SC_ENTRY + hh * C::SC_FLOATS;
-                    const float sa = se[q * 4 + j];
-                    float sc[NCH];
-#pragma unroll
-                    for (int x = 0; x < NCH; ++x) sc[x] = sa * se[16 + (h * NCH + x) * 4 + j];
+                    static_assert(NCH == 4, "one 16-byte load of column scales per K block");
+                    const float sa = se[j * 4 + q];
+                    const float4 sb = *reinterpret_cast<const float4 *>(se + 16 + j * NBB + h * NCH);
+                    const float sc[NCH] = {sa * sb.x, sa * sb.y, sa * sb.z, sa * sb.w};
                     if (++j == KB_PER_STAGE) {
                         j = 0;
                         if (++hh == C::HALVES) {
