@@ -24,8 +24,9 @@
 // as little as possible between MMAs.
 //
 // Roles (384 threads, one CTA per SM, persistent over output tiles; in a pair
-// each CTA runs every role on its half and the peer's MMA warp forwards its
-// readiness to the leader with relaxed cluster-scope arrives):
+// each CTA runs every role on its half: both CTAs' operand loads complete on
+// the leader's barriers (cta_group::2 TMA), and the peer's MMA warp forwards
+// the readiness of its scale lines with relaxed cluster-scope arrives):
 //   warp 0     producer: TMA loads of the A and B K-slices into a ring of
 //              shared-memory stages (128-byte swizzle; grouped problems: A
 //              rows by cp.async).
@@ -178,7 +179,7 @@ enum : int {
     TR_SCALE_BUILD = 12,    // scale warp: starting step `it`'s lines (before waiting for its copies)
     TR_MMA_SF_OK = 13,      // MMA lane 0: scale lines of stage `it` ready
     TR_MMA_FULL_OK = 14,    // MMA lane 0: own operand bytes of stage `it` landed
-    TR_PEER_FWD = 15,       // peer MMA warp: its bytes of stage `it` landed, forwarded
+    TR_PEER_FWD = 15,       // peer MMA warp: its scale lines of stage `it` forwarded
     TR_MMA_VOK = 16,        // MMA lane 0: verdict of tile `i` seen
     TR_MMA_T0 = 17,         // MMA lane 0: accumulator released by the local epilogue (tile `i`)
     TR_MMA_LOOP = 18,       // MMA lane 0: tile `i`'s K loop about to wait for its first scale entry
@@ -212,9 +213,9 @@ struct GroupedArgs {
 
 template <int STAGES, int SF_STAGES>
 struct Ctrl {
-    uint64_t full[STAGES];        // producer -> MMA warp (TMA bytes; grouped: + A-row cp.async)
+    uint64_t full[STAGES];        // producer -> MMA warp (TMA bytes; grouped: + A-row cp.async;
+                                  // pairs: both CTAs' bytes, on the leader's copy)
     uint64_t empty[STAGES];       // MMA commit -> producer
-    uint64_t pfwd[STAGES];        // CTA pairs: peer's stage landed (forwarded to the leader)
     uint64_t scfull[SF_STAGES];   // scale cp.async landed -> scale warp
     uint64_t sfready[SF_STAGES];  // scale warp -> MMA warp (lines written)
     uint64_t sfempty[SF_STAGES];  // MMA commit -> scale warp (lines and scales consumed)
@@ -521,7 +522,6 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             // arrival per producer lane
             mbar_init(&ctl->full[s], GROUPED ? 1 + 32 : 1);
             mbar_init(&ctl->empty[s], 1);
-            mbar_init(&ctl->pfwd[s], 1);
         }
         for (int f = 0; f < FS; ++f) {
             mbar_init(&ctl->scfull[f], 32);   // one cp.async arrival per scale-warp lane
@@ -633,30 +633,31 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             for (int ks = 0, k0 = 0; ks < KW; ++ks, k0 += C::HALVES * BK) {
                 ok = __all_sync(FULL, wait_bar(&ctl->empty[s], ph ^ 1u, ctl, c));
                 if (!ok) break;
-                if ((c.withhold_stage == it) && blockIdx.x == 0) {
+                if ((c.withhold_stage == it) && blockIdx.x < (PAIR ? 2u : 1u)) {
                     withheld = s;
                 } else {
                     if (lane == 0) {
                         trace_event(c, TR_PROD_ISSUE, it);
                         if constexpr (PAIR) {
-                            // each CTA's bytes complete on its own barrier; the peer's
-                            // MMA warp forwards its completion to the leader
+                            // both CTAs' loads complete on the leader's barrier
+                            // (cta_group::2), which the leader arms for the pair's bytes
                             const int ar = tt.m0 + row_off, br = tt.n0 + static_cast<int>(rank) * (BN / 2);
+                            const uint32_t bar_l = mapa_shared(&ctl->full[s], 0);   // the leader's barrier
                             if (k0 + 2 * BK <= c.K) {
                                 // both halves inside K: one box per operand
-                                mbar_arrive_expect_tx(&ctl->full[s], C::A_BYTES + C::B_BYTES);
-                                tma_load_3d(&args.tmA3, &ctl->full[s], sm_a + s * C::A_BYTES, 0, ar, k0 / BK);
-                                tma_load_3d(&args.tmB3, &ctl->full[s], sm_b + s * C::B_BYTES, 0, br, k0 / BK);
+                                if (leader) mbar_arrive_expect_tx(&ctl->full[s], 2 * (C::A_BYTES + C::B_BYTES));
+                                tma_load_3d_pair(&args.tmA3, bar_l, sm_a + s * C::A_BYTES, 0, ar, k0 / BK);
+                                tma_load_3d_pair(&args.tmB3, bar_l, sm_b + s * C::B_BYTES, 0, br, k0 / BK);
                             } else {
                                 // the tile's last stage: the halves that start before K,
                                 // from the 2D maps, which zero-fill K past the end
                                 const int nh = k0 + BK < c.K ? 2 : 1;
-                                mbar_arrive_expect_tx(&ctl->full[s], nh * (C::A_HALF + C::B_HALF));
+                                if (leader) mbar_arrive_expect_tx(&ctl->full[s], 2 * nh * (C::A_HALF + C::B_HALF));
                                 for (int hh = 0; hh < nh; ++hh) {
-                                    tma_load_2d(&args.tmA, &ctl->full[s], sm_a + s * C::A_BYTES + hh * C::A_HALF,
-                                                k0 + hh * BK, ar);
-                                    tma_load_2d(tmb, &ctl->full[s], sm_b + s * C::B_BYTES + hh * C::B_HALF,
-                                                k0 + hh * BK, br);
+                                    tma_load_2d_pair(&args.tmA, bar_l, sm_a + s * C::A_BYTES + hh * C::A_HALF,
+                                                     k0 + hh * BK, ar);
+                                    tma_load_2d_pair(tmb, bar_l, sm_b + s * C::B_BYTES + hh * C::B_HALF,
+                                                     k0 + hh * BK, br);
                                 }
                             }
                         } else {
@@ -691,7 +692,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             }
         }
         // drain: every armed stage's last phase must complete before the CTA exits
-        if (lane == 0) {
+        // (a pair's loads all complete on the leader's barriers)
+        if (lane == 0 && (!PAIR || leader)) {
             for (int d = max(0, it - S); d < it; ++d) {
                 const int sd = d % S;
                 if (sd == withheld) continue;
@@ -765,7 +767,6 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                             trace_event(c, TR_MMA_SF_OK, ot + w);
                             ok = ok && wait_spin(&ctl->full[s], ph, ctl, c);
                             trace_event(c, TR_MMA_FULL_OK, ot + w);
-                            ok = ok && (!PAIR || wait_spin(&ctl->pfwd[s], ph, ctl, c));
                             if (!ok) break;
                         }
                         next_ready = false;
@@ -798,8 +799,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                                         const uint32_t ph2 = s + 1 == S ? ph ^ 1u : ph;
                                         const uint32_t phf2 = f + 1 == FS ? phf ^ 1u : phf;
                                         next_ready = mbar_test_wait(&ctl->sfready[f2], phf2) &&
-                                                     mbar_test_wait(&ctl->full[s2], ph2) &&
-                                                     (!PAIR || mbar_test_wait(&ctl->pfwd[s2], ph2));
+                                                     mbar_test_wait(&ctl->full[s2], ph2);
                                     }
                                     mma_block<PAIR>(tmem, ad + static_cast<uint64_t>((hh * C::A_HALF >> 4) + 2 * j),
                                                     bd + static_cast<uint64_t>((hh * C::B_HALF >> 4) + 2 * j),
@@ -818,16 +818,12 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     if (ok) commit_to<PAIR>(&ctl->tfull[0]);
                 }
                 if (PAIR && !leader && lane == 0) {
-                    // forward each stage's scale lines and operand bytes to the
-                    // leader's MMA thread
+                    // forward each stage's scale lines to the leader's MMA thread
                     for (int w = 0; w < KW && ok; ++w) {
                         const int os = ot + w;
                         const int f = os % FS;
                         ok = wait_spin(&ctl->sfready[f], static_cast<uint32_t>(os / FS) & 1u, ctl, c);
                         if (ok) mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
-                        const int s = os % S;
-                        ok = ok && wait_spin(&ctl->full[s], static_cast<uint32_t>(os / S) & 1u, ctl, c);
-                        if (ok) mbar_signal_cluster(mapa_shared(&ctl->pfwd[s], 0));
                         trace_event(c, TR_PEER_FWD, os);
                     }
                 }
@@ -846,13 +842,11 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     const int s = os % S;
                     const int f = os % FS;
                     const uint32_t phs = static_cast<uint32_t>(os / S) & 1u;
-                    ok = __all_sync(FULL, wait_bar(&ctl->full[s], phs, ctl, c) &&
-                                              (!PAIR || !leader || wait_bar(&ctl->pfwd[s], phs, ctl, c)) &&
+                    ok = __all_sync(FULL, (PAIR && !leader ? true : wait_bar(&ctl->full[s], phs, ctl, c)) &&
                                               wait_bar(&ctl->sfready[f], static_cast<uint32_t>(os / FS) & 1u, ctl, c));
                     if (!ok) break;
                     if (PAIR && !leader && lane == 0 && hh == 0) {
                         mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
-                        mbar_signal_cluster(mapa_shared(&ctl->pfwd[s], 0));
                     }
                     if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
                     const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES + hh * C::A_HALF));

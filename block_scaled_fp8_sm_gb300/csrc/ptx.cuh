@@ -415,6 +415,15 @@ __device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint
 
 // TMA load into this CTA's shared memory that completes its bytes on an
 // mbarrier given by shared::cluster address (the pair leader's).
+__device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap *m, uint32_t bar_cluster, void *dst,
+                                                 int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap *m, uint32_t bar_cluster, void *dst,
                                                  int32_t c0, int32_t c1) {
     asm volatile(
