@@ -46,6 +46,7 @@ WORKLOAD_NAMES = {
     "c2": "prefill projection GEMM M=8192 N=28672 K=8192, pow2 32x32 scales",
     "c3": "grouped decode G=16 M_g~U[1,64] N=4096 K=7168, per-group B, pow2 scales",
     "c4": "arbitrary-scale GEMM M=N=K=8192 (amax/448 scales, 0.5% x50 outliers)",
+    "c4p": "arbitrary-scale GEMM M=N=K=8192 as c4, promotion path pinned (mode PROMOTE: single-CTA tiles)",
     "q8": "block quantization of bf16 activations 8192x8192 -> E4M3 codes + 32x32 fp32 scales",
     "r1": "per-token x per-channel scaled E4M3 GEMM M=N=K=4096 (fp32 scales [M] and [N]), bf16 out",
     "f1": "block-scaled E4M3 GEMM M=N=K=4096 with a bf16 residual added in the epilogue",
@@ -208,7 +209,7 @@ def make_runner(name, dev, bs):
         def run(stream):
             bs.fp8_gemm_rowcol(p.A, sA, p.B, sB, C, p.M, p.N, p.K, stream=stream)
         return run, p.flops, nbytes
-    p = workloads.make(name, seed=0, device=dev)
+    p = workloads.make("c4" if name == "c4p" else name, seed=0, device=dev)
     if name == "c3":
         Cs = [torch.empty(m, p.N, dtype=torch.bfloat16, device=dev) for m in p.Ms]
         groups = [(p.A[o:o + m], sa, b, sb, c) for o, m, sa, b, sb, c in
@@ -219,9 +220,10 @@ def make_runner(name, dev, bs):
             bs.fp8_gemm_grouped(groups, Ms, p.N, p.K, stream=stream)
         return run, p.flops, p.algorithmic_bytes
     C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
+    mode = 2 if name == "c4p" else None   # FP8_PATH_PROMOTE
 
     def run(stream):
-        bs.fp8_gemm_blockscaled(p.A, p.sA, p.B, p.sB, C, p.M, p.N, p.K, stream=stream)
+        bs.fp8_gemm_blockscaled(p.A, p.sA, p.B, p.sB, C, p.M, p.N, p.K, stream=stream, mode=mode)
     return run, p.flops, p.algorithmic_bytes
 
 
@@ -402,7 +404,7 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     results = {}
-    names = [HEADLINE] + ([] if args.headline_only else ["c2", "c3", "c4", "q8", "r1", "f1"])
+    names = [HEADLINE] + ([] if args.headline_only else ["c2", "c3", "c4", "c4p", "q8", "r1", "f1"])
     if args.only:
         names = [args.only]
     with ClockSampler(local) as clk:
@@ -552,7 +554,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-elements", type=int, default=65536)
-    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "q8", "r1", "f1"], default=None,
+    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "c4p", "q8", "r1", "f1"], default=None,
                     help="time one workload only (no e2e, no CPU baseline): profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -479,6 +479,9 @@ int fp8_gemm_blockscaled_ex(const void *A, const float *sA, const void *B, const
     rc = device_setup(&d);
     if (rc != FP8_OK) return rc;
     if (K == 0) return zero_fill(C, M * N, stream);
+    // Every tile promotes: the single-CTA kernel, whose promotion pipeline
+    // waits on no cross-CTA releases, runs this path faster than CTA pairs.
+    if (mode == FP8_PATH_PROMOTE) return launch_plain<TILE_N>(A, sA, B, sB, C, M, N, K, mode, d, stream);
     return launch_pair<TILE_N>(A, sA, B, sB, C, M, N, K, mode, d, stream);
 }
 

@@ -66,16 +66,19 @@ enum {
 };
 
 /* Path selection.
- * FP8_PATH_AUTO: per output tile (128 rows x BN columns), the native path is
+ * FP8_PATH_AUTO: per output tile (256 rows x 256 columns), the native path is
  *   taken when every scale the tile reads (its row blocks of sA and column
  *   blocks of sB, all of K) is a positive normal power of two; otherwise the
  *   promotion path.  A row's bits therefore depend only on the scales of the
- *   rows in its own 128-row tile (rows 128*floor(m/128) ...).
+ *   rows in its own 256-row tile (rows 256*floor(m/256) ...).
  * FP8_PATH_NATIVE: block-scaled tensor-core path (kind::mxf8f6f4 with UE8M0
  *   scales, exact for power-of-two scales).  A tile that finds another scale
  *   is computed by the promotion path and FP8_ERR_SCALE is recorded.
  * FP8_PATH_PROMOTE: per-K-block fp32 promotion for arbitrary fp32 scales:
- *   unscaled 32-deep tensor-core partials, scaled and accumulated in fp32. */
+ *   unscaled 32-deep tensor-core partials, scaled and accumulated in fp32.
+ *   Runs on single-CTA 128 x 256 tiles (faster for this path than CTA
+ *   pairs); each element equals, bit for bit, what AUTO computes for it on a
+ *   promoted tile. */
 enum { FP8_PATH_AUTO = 0, FP8_PATH_NATIVE = 1, FP8_PATH_PROMOTE = 2 };
 
 /* Block-scaled GEMM, AUTO path.  Returns FP8_OK or FP8_ERR_*.
