@@ -15,7 +15,9 @@
 //                       variants for per-row/column scales and a fused
 //                       residual add
 //   bsfp8_gemm_plain    single problems, one CTA per 128 x 256 tile (the
-//                       allocation-free entry point)
+//                       allocation-free entry point, and the promotion path
+//                       when the caller pins it: with no cross-CTA releases
+//                       per 32-K partial it runs that path faster)
 //   bsfp8_gemm_grouped  many decode problems in one launch: 64-row tiles, A
 //                       rows by cp.async (their count lives on the device)
 // An M=128 MMA costs ~116 cycles for any N <= 128 but only ~160 for N = 256,
