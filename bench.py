@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -63,13 +64,22 @@ def peaks():
     return p, src
 
 
+def _code_only(src):
+    """The source without comments and blank lines (no string literal in the
+    CUDA sources holds a comment marker), so that editing a comment does not
+    count as a kernel change."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.split("\n") if line.strip())
+
+
 def source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_fp8_sm_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
