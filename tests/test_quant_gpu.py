@@ -76,3 +76,39 @@ def test_quantized_operands_feed_the_gemm(bs):
     q_ref, s_ref = oracle.quantize_blocks(_bits(xb), M, K)
     Cr, T = oracle.gemm(q_ref, s_ref, B.numpy(), sB.numpy(), M, N, K)
     check(bf16_to_f64(C), Cr, T, "quantize -> gemm")
+
+
+def test_quantize_rounding_midpoints(bs):
+    """Quotients x / s that are E4M3 rounding midpoints (exact ties, which
+    round to the even code) or lie just above one, with scales whose
+    reciprocal is inexact (s = 3, 5, 7, 1.5): a reciprocal product instead of
+    the correctly rounded division would give 234 wrong codes on this data."""
+    rng = np.random.default_rng(21)
+    # E4M3 midpoints: normal (1 + (2j+1)/16) * 2^e, e in [-6, 8], and subnormal (2j+1) * 2^-10
+    mids = [(1 + (2 * j + 1) / 16) * 2.0 ** e for e in range(-6, 8) for j in range(8)]
+    mids += [(2 * j + 1) * 2.0 ** -10 for j in range(8)]
+    mids = np.array(mids)
+    blocks = []
+    for k in (3.0, 5.0, 7.0, 1.5):
+        blk = np.empty((32, 32))
+        vals = rng.choice(mids, size=32 * 32) * k * rng.choice([-1.0, 1.0], size=32 * 32)
+        blk[:] = vals.reshape(32, 32)
+        blk[0, 0] = 448.0 * k                      # the block maximum: s = k exactly
+        blocks.append(blk)
+    x = torch.from_numpy(np.concatenate(blocks, axis=1)).to(torch.float32)   # 32 x 128
+    xb = x.to(torch.bfloat16)
+    # the chosen values are exact in bf16 (few significant bits), so x / s are the midpoints
+    assert torch.equal(xb.to(torch.float32), x)
+    # neighbours one bf16 step away: quotients just off the midpoints
+    up = (xb.view(torch.int16) + 1).view(torch.bfloat16)
+    both = torch.cat([xb, up], dim=0)                                       # 64 x 128
+    both[32, 0] = xb[0, 0]
+    both[32, 32] = xb[0, 32]
+    both[32, 64] = xb[0, 64]
+    both[32, 96] = xb[0, 96]
+    M, K = both.shape
+    q, s = bs.fp8_quantize_blocks(both.to(DEV))
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quantize_blocks(_bits(both.contiguous()), M, K)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), q_ref)
