@@ -716,6 +716,17 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         // has been read); entries wait here, oldest first, with the index of
         // their last partial.
         int pend_f0 = -1, pend_l0 = 0, pend_f1 = -1, pend_l1 = 0;
+        // A pair's peer: in promotion tiles its epilogue releases a partial on
+        // its own barrier only, and this warp, which waits there anyway,
+        // forwards the release to the leader as one arrival counting for the
+        // peer's eight warps (bit b: buffer b's last use still to forward).
+        uint32_t fwd = 0;
+        auto forward_release = [&](uint32_t b) {
+            if (PAIR && !leader && ((fwd >> b) & 1u)) {
+                if (lane == 0) mbar_signal_cluster_count(mapa_shared(&ctl->tempty[b], 0), NUM_EPI_WARPS);
+                fwd &= ~(1u << b);
+            }
+        };
         auto release_read = [&](int upto) {   // partials <= upto have been read
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
@@ -740,6 +751,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 ok = __all_sync(FULL, wait_bar(&ctl->tempty[0], (uses0 & 1u) ^ 1u, ctl, c) &&
                                           wait_bar(&ctl->tempty[1], (uses1 & 1u) ^ 1u, ctl, c));
                 if (!ok) break;
+                forward_release(0u);
+                forward_release(1u);
                 release_read(static_cast<int>(pk));
             }
             if (!promote) {
@@ -859,6 +872,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         const uint32_t ub = b ? uses1 : uses0;
                         ok = __all_sync(FULL, wait_bar(&ctl->tempty[b], (ub & 1u) ^ 1u, ctl, c));
                         if (!ok) break;
+                        forward_release(b);
                         release_read(static_cast<int>(pk) - 2);
                         if (lane == 0) {
                             if (leader) {
@@ -876,6 +890,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         }
                         issued = true;
                         if (b) ++uses1; else ++uses0;
+                        fwd |= 1u << b;
                         ++pk;
                     }
                     if (!ok) break;
@@ -1227,10 +1242,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         if (x == 2 * NCH - 1) {
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) {
-                                mbar_arrive(&ctl->tempty[b]);
-                                if (PAIR && !leader) mbar_signal_cluster(mapa_shared(&ctl->tempty[b], 0));
-                            }
+                            // (a pair's peer: its MMA warp forwards the release)
+                            if (lane == 0) mbar_arrive(&ctl->tempty[b]);
                         }
 #pragma unroll
                         for (int y = 0; y < 16; ++y)

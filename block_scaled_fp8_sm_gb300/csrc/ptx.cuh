@@ -352,6 +352,12 @@ __device__ __forceinline__ void mbar_signal_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// The same signal counting as `count` arrivals.
+__device__ __forceinline__ void mbar_signal_cluster_count(uint32_t cluster_addr, uint32_t count) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr), "r"(count)
+                 : "memory");
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
