@@ -173,6 +173,33 @@ def test_batch_invariance_bit_exact(bs, name, sizes):
         assert torch.equal(rows[m][:k], ref[:k]), f"M={m} differs"
 
 
+def test_batch_invariance_pinned_promotion(bs):
+    """With the promotion path pinned (single-CTA tiles), the first rows are
+    bit-identical across launches of different M, and equal to what AUTO
+    computes for them when their tile promotes (the 8192^3 outlier data)."""
+    p = workloads.make("c4", seed=0, device=DEV)
+    N, K = 512, 2048   # a slice of the outlier problem: B rows and K columns prefixes
+    B = p.B[:N, :K].contiguous()
+    sB = p.sB[:N // 32, :K // 32].contiguous()
+    rows = {}
+    for m in (1, 7, 64, 300):
+        A = p.A[:m, :K].contiguous()
+        sA = p.sA[:(m + 31) // 32, :K // 32].contiguous()
+        C = torch.empty(m, N, dtype=torch.bfloat16, device=DEV)
+        bs.fp8_gemm_blockscaled(A, sA, B, sB, C, m, N, K, mode=2)
+        torch.cuda.synchronize()
+        rows[m] = C[:64].view(torch.int16).clone()
+        if m == 300:
+            Ca = torch.empty(m, N, dtype=torch.bfloat16, device=DEV)
+            bs.fp8_gemm_blockscaled(A, sA, B, sB, Ca, m, N, K)
+            torch.cuda.synchronize()
+            assert torch.equal(Ca.view(torch.int16), C.view(torch.int16)), "AUTO vs pinned promotion"
+    for m in (1, 7, 64):
+        k = min(m, 64)
+        assert torch.equal(rows[m][:k], rows[300][:k]), f"M={m} differs"
+    assert bs.fp8_status_query() == 0
+
+
 # ------------------------------------------------------------------- grouped
 
 def _grouped_run(bs, gp, mode=None):
