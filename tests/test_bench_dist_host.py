@@ -75,3 +75,23 @@ def test_reference_arm_prints_on_rank0_only(rank):
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_source_hash_ignores_comments_only():
+    bench = _bench()
+    code = "int f(int x) {\n    return x + 1;   // one more\n}\n/* block\n comment */\n"
+    assert bench._code_only(code) == bench._code_only("int f(int x) {\n    return x + 1;\n}\n")
+    assert bench._code_only(code) != bench._code_only("int f(int x) {\n    return x + 2;\n}\n")
+
+
+def test_traffic_reported_only_for_the_captured_source(tmp_path, monkeypatch):
+    bench = _bench()
+    rec = {"source_hash": bench.source_hash(), "c1": {"dram_bytes_per_launch": 123, "source_hash": bench.source_hash()},
+           "c2": {"dram_bytes_per_launch": 456, "source_hash": "0000000000000000"}}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC", str(path))
+    assert bench.recorded_traffic("c1") == 123     # captured on this source
+    assert bench.recorded_traffic("c2") is None    # another kernel source
+    assert bench.recorded_traffic("c3") is None    # never captured
+
