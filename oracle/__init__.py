@@ -71,6 +71,12 @@ def _load():
         lib.oracle_gemm_rowcol.restype = ctypes.c_int
         lib.oracle_quantize_blocks.argtypes = [dp, i64, i64, u8p, fp]
         lib.oracle_quantize_blocks.restype = ctypes.c_int
+        lib.oracle_gemm_residual.argtypes = [u8p, fp, u8p, fp, dp, i64, i64, i64, dp, dp,
+                                             ctypes.c_int, ctypes.c_int]
+        lib.oracle_gemm_residual.restype = ctypes.c_int
+        lib.oracle_gemm_residual_sampled.argtypes = [u8p, fp, u8p, fp, dp, i64, i64, i64,
+                                                     dp, dp, i64, dp, dp, ctypes.c_int]
+        lib.oracle_gemm_residual_sampled.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -199,4 +205,57 @@ def gemm_rowcol(A, sA, B, sB, M: int, N: int, K: int):
     T = np.empty((M, N), dtype=np.float64)
     if _load().oracle_gemm_rowcol(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), M, N, K, _ptr(C), _ptr(T)) != 0:
         raise ValueError("oracle_gemm_rowcol: bad arguments")
+    return C, T
+
+
+def _bf16_bits(R, M: int, N: int) -> np.ndarray:
+    a = np.asarray(R)
+    if a.dtype not in (np.uint16, np.int16):
+        raise ValueError(f"bf16 bit patterns must be uint16 or int16, got {a.dtype}")
+    a = np.ascontiguousarray(a.view(np.uint16))
+    if a.size != M * N:
+        raise ValueError(f"expected {M}x{N} bf16 bit patterns, got {a.shape}")
+    return a.reshape(M, N)
+
+
+def gemm_residual(A, sA, B, sB, R_bits, M: int, N: int, K: int, nthreads: int = 0,
+                  mutation: int = 0):
+    """C = block-scaled GEMM + R with R given as bf16 bit patterns (uint16 or
+    int16 [M, N]); returns (C, T) in fp64, T the GEMM's magnitude sum.
+    ``mutation`` != 0 plants a known mistake (tests of the pins only)."""
+    KB = K // 32
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    A = _codes(A, M, K)
+    B = _codes(B, N, K)
+    sA = _scales(sA, M, KB)
+    sB = _scales(sB, N, KB)
+    R = _bf16_bits(R_bits, M, N)
+    C = np.zeros((M, N), dtype=np.float64)
+    T = np.zeros((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_residual(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(R), M, N, K,
+                                      _ptr(C), _ptr(T), int(nthreads), int(mutation))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_residual failed ({rc})")
+    return C, T
+
+
+def gemm_residual_sampled(A, sA, B, sB, R_bits, M: int, N: int, K: int, ms, ns, nthreads: int = 0):
+    """gemm_residual at the sampled coordinates (ms[i], ns[i])."""
+    KB = K // 32
+    A = _codes(A, M, K)
+    B = _codes(B, N, K)
+    sA = _scales(sA, M, KB)
+    sB = _scales(sB, N, KB)
+    R = _bf16_bits(R_bits, M, N)
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    if ms.shape != ns.shape:
+        raise ValueError("ms and ns differ in shape")
+    C = np.zeros(ms.shape, dtype=np.float64)
+    T = np.zeros(ms.shape, dtype=np.float64)
+    rc = _load().oracle_gemm_residual_sampled(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(R), M, N, K,
+                                              _ptr(ms), _ptr(ns), ms.size, _ptr(C), _ptr(T), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_residual_sampled failed ({rc})")
     return C, T

@@ -324,3 +324,45 @@ int oracle_gemm_rowcol(const uint8_t *A, const float *sA, const uint8_t *B, cons
     }
     return 0;
 }
+
+/* --------------------------------------------------- GEMM + residual ---- */
+
+/* The block-scaled GEMM above followed by a bf16 residual added to each
+ * output element (FP8 GEMM library article, hncyxsy.com/news/241433, section
+ * 2.3: element-wise tail work belongs in the GEMM's epilogue instead of a
+ * separate pass; section 5, pitfall 4, names the residual / LayerNorm fusion):
+ *
+ *   C[m,n] = sum_kb sA[m/32][kb] * sB[n/32][kb] * sum_{k in kb} A[m,k] * B[n,k]  +  R[m,n]
+ *
+ * R is bf16 [M, N] row-major, given as its 16-bit patterns; its value is exact
+ * in fp64, and the GEMM value is the one oracle_gemm returns, so the sum is
+ * the only extra rounding.  T is the GEMM's magnitude sum, unchanged.
+ * `mutation` plants a known mistake for the pin tests only (0: none; 4: the
+ * residual is left out; 5: the residual of column (n+1) mod N is added). */
+static double residual_term(const uint16_t *R, int64_t N, int64_t m, int64_t n, int mutation) {
+    if (mutation == 4) return 0.0;
+    if (mutation == 5) n = (n + 1) % N;
+    return oracle_bf16_value(R[m * N + n]);
+}
+
+int oracle_gemm_residual(const uint8_t *A, const float *sA, const uint8_t *B, const float *sB,
+                         const uint16_t *R, int64_t M, int64_t N, int64_t K, double *C, double *T,
+                         int nthreads, int mutation) {
+    const int rc = oracle_gemm(A, sA, B, sB, M, N, K, C, T, nthreads, 0);
+    if (rc != 0) return rc;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            C[m * N + n] += residual_term(R, N, m, n, mutation);
+    return 0;
+}
+
+/* The same at the sampled coordinates (ms[i], ns[i]) for i < count. */
+int oracle_gemm_residual_sampled(const uint8_t *A, const float *sA, const uint8_t *B, const float *sB,
+                                 const uint16_t *R, int64_t M, int64_t N, int64_t K,
+                                 const int64_t *ms, const int64_t *ns, int64_t count,
+                                 double *C, double *T, int nthreads) {
+    const int rc = oracle_gemm_sampled(A, sA, B, sB, M, N, K, ms, ns, count, C, T, nthreads);
+    if (rc != 0) return rc;
+    for (int64_t i = 0; i < count; ++i) C[i] += residual_term(R, N, ms[i], ns[i], 0);
+    return 0;
+}

@@ -489,3 +489,65 @@ def test_rowcol_operand_swap_symmetry():
     C, _ = oracle.gemm_rowcol(A, sA, B, sB, M, N, K)
     Ct, _ = oracle.gemm_rowcol(B, sB, A, sA, N, M, K)
     assert np.array_equal(C, Ct.T)
+
+
+# -------------------------------------------------------- GEMM + residual ----
+
+def _bf16_bits_of(x):
+    """bf16 bit patterns of fp32 values via torch's cast (not the oracle)."""
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+
+
+def test_residual_zero_reduces_to_gemm():
+    M, N, K = 45, 64, 160
+    A, sA, B, sB = _rand_problem(M, N, K, seed=21, arbitrary=True)
+    R = np.zeros((M, N), dtype=np.uint16)
+    C0, T0 = oracle.gemm(A, sA, B, sB, M, N, K)
+    C1, T1 = oracle.gemm_residual(A, sA, B, sB, R, M, N, K)
+    assert np.array_equal(C0, C1) and np.array_equal(T0, T1)
+    # -0.0 (0x8000) is a zero residual too
+    C2, _ = oracle.gemm_residual(A, sA, B, sB, np.full((M, N), 0x8000, np.uint16), M, N, K)
+    assert np.array_equal(C0, C2)
+
+
+def _identity_case(M, K, seed):
+    A, _, _, _ = _rand_problem(M, K, K, seed=seed)
+    B = np.zeros((K, K), dtype=np.uint8)
+    B[np.arange(K), np.arange(K)] = 0x38                          # 1.0
+    ones_a = np.ones(((M + 31) // 32, K // 32), np.float32)
+    ones_b = np.ones((K // 32, K // 32), np.float32)
+    rng = np.random.default_rng(seed)
+    R = _bf16_bits_of(rng.standard_normal((M, K)) * 30)
+    # closed form from torch's own decodings: C = A + R, one fp64 rounding
+    a = torch.from_numpy(A).view(torch.float8_e4m3fn).to(torch.float64)
+    r = torch.from_numpy(R).view(torch.bfloat16).to(torch.float64)
+    return A, ones_a, B, ones_b, R, (a + r).numpy()
+
+
+def test_residual_identity_weights_closed_form():
+    M, K = 70, 96
+    A, sA, B, sB, R, exp = _identity_case(M, K, seed=22)
+    C, _ = oracle.gemm_residual(A, sA, B, sB, R, M, K, K)
+    assert np.array_equal(C, exp)
+
+
+@pytest.mark.parametrize("mutation", [4, 5])
+def test_residual_planted_mistakes_are_caught(mutation):
+    """A dropped residual or one taken from the wrong column fails the
+    identity-weights closed form."""
+    M, K = 40, 64
+    A, sA, B, sB, R, exp = _identity_case(M, K, seed=23)
+    C, _ = oracle.gemm_residual(A, sA, B, sB, R, M, K, K, mutation=mutation)
+    assert not np.array_equal(C, exp)
+
+
+def test_residual_sampled_equals_full():
+    M, N, K = 77, 96, 128
+    A, sA, B, sB = _rand_problem(M, N, K, seed=24, arbitrary=True)
+    R = _bf16_bits_of(np.random.default_rng(24).standard_normal((M, N)) * 5)
+    C, T = oracle.gemm_residual(A, sA, B, sB, R, M, N, K)
+    rng = np.random.default_rng(25)
+    ms = rng.integers(0, M, 300)
+    ns = rng.integers(0, N, 300)
+    Cs, Ts = oracle.gemm_residual_sampled(A, sA, B, sB, R, M, N, K, ms, ns)
+    assert np.array_equal(Cs, C[ms, ns]) and np.array_equal(Ts, T[ms, ns])

@@ -1,7 +1,11 @@
 """GPU parity of the block-scaled GEMM with a fused residual add
-(fp8_gemm_blockscaled_residual, through the C ABI): C = bf16(GEMM + R), the
-GEMM from the CPU oracle and R added in fp64.  Tolerance: tests/_accept.py
-with the GEMM's magnitude sum T (R is exact in fp32 and adds one rounding)."""
+(fp8_gemm_blockscaled_residual, through the C ABI): C = bf16(GEMM + R)
+against the oracle's GEMM + residual (oracle_gemm_residual), element by
+element.  Tolerance: tests/_accept.py with the GEMM's magnitude sum T (R is
+exact in fp32 and adds one rounding).  Besides small and ragged shapes, the
+4096^3 problem the benchmark times (256 tiles on 76 CTA pairs, so every CTA
+runs several tiles and reuses its residual staging buffer) is compared on
+sampled elements and whole rows, out of place and in place, on both paths."""
 import numpy as np
 import pytest
 import torch
@@ -38,8 +42,8 @@ def _problem(M, N, K, seed, arbitrary=False):
 
 
 def _expected(A, sA, B, sB, R, M, N, K):
-    Cr, T = oracle.gemm(A.numpy(), sA.numpy(), B.numpy(), sB.numpy(), M, N, K)
-    return Cr + R.float().numpy().astype(np.float64), T
+    return oracle.gemm_residual(A.numpy(), sA.numpy(), B.numpy(), sB.numpy(),
+                                R.view(torch.int16).numpy(), M, N, K)
 
 
 @pytest.mark.parametrize("M,N,K,arbitrary", [(1, 32, 64, False), (77, 288, 544, False), (300, 512, 1024, False),
@@ -83,3 +87,58 @@ def test_residual_zero_equals_plain_bits(bs):
     bs.fp8_gemm_blockscaled_residual(*d, torch.zeros(M, N, dtype=torch.bfloat16, device=DEV), C2, M, N, K)
     torch.cuda.synchronize()
     assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+
+
+# ------------------------------------------------- multi-tile (bench size)
+
+def _bench_size_problem(arbitrary):
+    """The 4096^3 square workload (power-of-two scales), or the same codes
+    with arbitrary fp32 scales (every tile promotes), plus a seeded bf16
+    residual; generated on the device like the benchmark's inputs."""
+    p = workloads.make("c1", seed=0, device=DEV)
+    if arbitrary:
+        g = torch.Generator(device=DEV).manual_seed(7)
+        p.sA = torch.rand(p.sA.shape, generator=g, device=DEV) * 2 + 0.05
+        p.sB = torch.rand(p.sB.shape, generator=g, device=DEV) * 2 + 0.05
+    g = torch.Generator(device=DEV).manual_seed(1)
+    R = torch.randn(p.M, p.N, generator=g, device=DEV).to(torch.bfloat16)
+    return p, R
+
+
+def _sampled_residual_check(p, R, C, what, n_samples=6000):
+    rng = np.random.default_rng(3)
+    rows = (0, 255, 256, p.M - 1)
+    ms = np.concatenate([rng.integers(0, p.M, n_samples)] + [np.full(p.N, r) for r in rows])
+    ns = np.concatenate([rng.integers(0, p.N, n_samples)] + [np.arange(p.N) for _ in rows])
+    A, sA, B, sB = (t.cpu().numpy() for t in (p.A, p.sA, p.B, p.sB))
+    Cr, T = oracle.gemm_residual_sampled(A, sA, B, sB, R.cpu().view(torch.int16).numpy(),
+                                         p.M, p.N, p.K, ms, ns)
+    Cg = C[torch.from_numpy(ms).to(DEV), torch.from_numpy(ns).to(DEV)]
+    check(bf16_to_f64(Cg), Cr, T, what)
+
+
+@pytest.mark.parametrize("arbitrary", [False, True])
+def test_residual_bench_size_multi_tile(bs, arbitrary):
+    p, R = _bench_size_problem(arbitrary)
+    buf = torch.full((p.M + 2, p.N), -7.0, dtype=torch.bfloat16, device=DEV)
+    C = buf[1:p.M + 1]
+    bs.fp8_gemm_blockscaled_residual(p.A, p.sA, p.B, p.sB, R, C, p.M, p.N, p.K)
+    torch.cuda.synchronize()
+    assert torch.all(buf[0] == -7.0) and torch.all(buf[-1] == -7.0), "store outside C"
+    assert bs.fp8_status_query() == 0
+    _sampled_residual_check(p, R, C, f"residual 4096^3{' arb' if arbitrary else ''}")
+
+
+@pytest.mark.parametrize("arbitrary", [False, True])
+def test_residual_bench_size_in_place(bs, arbitrary):
+    p, R = _bench_size_problem(arbitrary)
+    C = R.clone()
+    bs.fp8_gemm_blockscaled_residual(p.A, p.sA, p.B, p.sB, C, C, p.M, p.N, p.K)
+    torch.cuda.synchronize()
+    assert bs.fp8_status_query() == 0
+    _sampled_residual_check(p, R, C, f"residual 4096^3 in place{' arb' if arbitrary else ''}")
+    # in place and out of place give the same bits
+    C2 = torch.empty_like(C)
+    bs.fp8_gemm_blockscaled_residual(p.A, p.sA, p.B, p.sB, R, C2, p.M, p.N, p.K)
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
