@@ -2,18 +2,20 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step = one block-scaled GEMM of the headline workload (M=N=K=4096,
-power-of-two 32x32 scales, bf16 out) with inputs resident in HBM; the L2 is
-flushed (a 512 MiB write) between timed steps and each step is timed with CUDA
-events on the launching stream.  The same JSON line also carries the other
-workloads measured the same way: the 8192x28672x8192 prefill projection, the
-grouped decode batch (G=16, M_g in [1,64], N=4096, K=7168; GB/s against HBM;
-also as a CUDA-graph replay; its 470 MB of weights per step exceed the L2, so
-it runs without the flush, and its flushed time is reported beside it), the
-8192^3 arbitrary-scale GEMM with outliers (promotion path; also with the path
-pinned), the block quantization of 8192x8192 bf16 activations (GB/s against
-HBM), the 4096^3 GEMM with per-token x per-channel scales and the 4096^3 GEMM
-with a fused residual add.
+One step = one block-scaled GEMM of the headline workload, the prefill
+projection M=8192, N=28672, K=8192 (power-of-two 32x32 scales, bf16 out), with
+inputs resident in HBM; the L2 is flushed (a 512 MiB write) between timed
+steps and each step is timed with CUDA events on the launching stream.  The
+same JSON line also carries the other workloads measured the same way: the
+M=N=K=4096 square GEMM, the grouped decode batch (G=16, M_g in [1,64], N=4096,
+K=7168; GB/s against HBM; also as a CUDA-graph replay; its 470 MB of weights
+per step exceed the L2, so it runs without the flush, and its read-flushed and
+write-flushed times are reported beside it), the 8192^3 arbitrary-scale GEMM
+with outliers (promotion path; also with the path pinned), the block
+quantization of 8192x8192 bf16 activations (GB/s against HBM), the 4096^3 GEMM
+with per-token x per-channel scales and the 4096^3 GEMM with a fused residual
+add.  Every generated input buffer is recorded by its SHA-256, with the torch
+version that generated it.
 
 ``--impl reference`` times the CPU oracle (the only other implementation of
 the method; plain C, fp64) on a bounded sample of the same workload.
@@ -43,7 +45,8 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 FP8_PER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 L2_FLUSH_BYTES = 512 << 20
 
-HEADLINE = "c1"
+HEADLINE = "c2"
+HEADLINE_SHAPE = {"M": 8192, "N": 28672, "K": 8192}
 WORKLOAD_NAMES = {
     "c1": "block-scaled E4M3 GEMM M=N=K=4096, pow2 32x32 scales, bf16 out",
     "c2": "prefill projection GEMM M=8192 N=28672 K=8192, pow2 32x32 scales",
@@ -186,9 +189,18 @@ def max_over_ranks(x, world):
 
 # ----------------------------------------------------------------- ours ----
 
+def sha256_of(t):
+    """SHA-256 of a tensor's bytes (a list of tensors: of their bytes in order)."""
+    import torch
+    h = hashlib.sha256()
+    for x in (t if isinstance(t, (list, tuple)) else [t]):
+        h.update(x.detach().contiguous().view(-1).view(torch.uint8).cpu().numpy().tobytes())
+    return h.hexdigest()
+
+
 def make_runner(name, dev, bs):
-    """Returns (run(stream), flops, algorithmic bytes) for one workload with
-    its inputs on the device."""
+    """Returns (run(stream), flops, algorithmic bytes, input buffers) for one
+    workload with its inputs on the device."""
     import torch
 
     import workloads
@@ -203,15 +215,16 @@ def make_runner(name, dev, bs):
 
         def run(stream):
             bs.fp8_quantize_blocks(x, q, sc, stream=stream)
-        return run, 0, nbytes
+        return run, 0, nbytes, {"x": x}
     if name == "f1":
         p = workloads.make("c1", seed=0, device=dev)
-        R = torch.randn(p.M, p.N, device=dev).to(torch.bfloat16)
+        g = torch.Generator(device=dev).manual_seed(1)
+        R = torch.randn(p.M, p.N, generator=g, device=dev).to(torch.bfloat16)
         C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
 
         def run(stream):
             bs.fp8_gemm_blockscaled_residual(p.A, p.sA, p.B, p.sB, R, C, p.M, p.N, p.K, stream=stream)
-        return run, p.flops, p.algorithmic_bytes + 2 * p.M * p.N
+        return run, p.flops, p.algorithmic_bytes + 2 * p.M * p.N, {"A": p.A, "sA": p.sA, "B": p.B, "sB": p.sB, "R": R}
     if name == "r1":
         p = workloads.make("c1", seed=0, device=dev)
         g = torch.Generator(device=dev).manual_seed(1)
@@ -222,7 +235,7 @@ def make_runner(name, dev, bs):
 
         def run(stream):
             bs.fp8_gemm_rowcol(p.A, sA, p.B, sB, C, p.M, p.N, p.K, stream=stream)
-        return run, p.flops, nbytes
+        return run, p.flops, nbytes, {"A": p.A, "sA": sA, "B": p.B, "sB": sB}
     p = workloads.make("c4" if name == "c4p" else name, seed=0, device=dev)
     if name == "c3":
         Cs = [torch.empty(m, p.N, dtype=torch.bfloat16, device=dev) for m in p.Ms]
@@ -232,25 +245,27 @@ def make_runner(name, dev, bs):
 
         def run(stream):
             bs.fp8_gemm_grouped(groups, Ms, p.N, p.K, stream=stream)
-        return run, p.flops, p.algorithmic_bytes
+        return run, p.flops, p.algorithmic_bytes, {"A": p.A, "sA": p.sA, "B": p.B, "sB": p.sB, "Ms": Ms}
     C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
     mode = 2 if name == "c4p" else None   # FP8_PATH_PROMOTE
 
     def run(stream):
         bs.fp8_gemm_blockscaled(p.A, p.sA, p.B, p.sB, C, p.M, p.N, p.K, stream=stream, mode=mode)
-    return run, p.flops, p.algorithmic_bytes
+    return run, p.flops, p.algorithmic_bytes, {"A": p.A, "sA": p.sA, "B": p.B, "sB": p.sB}
 
 
 # The grouped decode streams 470 MB of weights per step, well above the 129 MB
 # L2, so it is timed without the write-flush: the flush leaves L2 full of dirty
 # lines whose write-back then lands inside an HBM-bound kernel (~129 MB of
 # extra DRAM writes per step); a GEMM of the square or prefill size is not
-# affected, the decode loses ~11 %.  Its flushed time is reported beside it.
+# affected, the decode loses ~11 %.  Its read-flushed time (a 512 MiB read
+# leaves L2 holding clean lines) and write-flushed time are reported beside it.
 UNFLUSHED = ("c3",)
 
 
-def time_device(run, steps, warmup, dev, flush_buf, world, flush=True):
-    """Per-step kernel time (ms) with CUDA events on the launching stream."""
+def time_device(run, steps, warmup, dev, flush_buf, world, flush="write"):
+    """Per-step kernel time (ms) with CUDA events on the launching stream.
+    flush: "write" (a 512 MiB fill), "read" (a 512 MiB reduction) or None."""
     import torch
     stream = torch.cuda.current_stream(dev)
     for _ in range(warmup):
@@ -258,11 +273,14 @@ def time_device(run, steps, warmup, dev, flush_buf, world, flush=True):
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
+    sink = torch.empty((), dtype=torch.int64, device=dev)
     barrier(world)
     torch.cuda.synchronize(dev)
     for i in range(steps):
-        if flush:
+        if flush == "write":
             flush_buf.fill_(i & 0xFF)      # evict the operands from L2
+        elif flush == "read":
+            torch.sum(flush_buf.view(torch.int64), out=sink)
         ev[i][0].record(stream)
         run(stream)
         ev[i][1].record(stream)
@@ -379,6 +397,60 @@ def time_e2e(name, steps, warmup, dev, bs, world):
     return ms, p.flops, h2d, d2h
 
 
+def time_e2e_grouped(steps, warmup, dev, bs, world):
+    """Grouped decode end to end, as a decode server runs it: the weights (B,
+    sB) stay resident in HBM; every step copies the batch's activation rows,
+    their scales and the row counts from pinned host memory, launches through
+    the public API and copies every group's output back."""
+    import torch
+
+    import workloads
+    p = workloads.make("c3", seed=0, device="cpu")
+    dB = [b.to(dev) for b in p.B]
+    dsB = [s.to(dev) for s in p.sB]
+    hA = p.A.pin_memory()
+    hsA = [s.pin_memory() for s in p.sA]
+    hMs = torch.tensor(p.Ms, dtype=torch.int32).pin_memory()
+    dA = torch.empty_like(hA, device=dev)
+    dsA = [torch.empty_like(s, device=dev) for s in hsA]
+    dMs = torch.empty_like(hMs, device=dev)
+    total = sum(p.Ms)
+    dC = torch.empty(total, p.N, dtype=torch.bfloat16, device=dev)
+    hC = torch.empty(total, p.N, dtype=torch.bfloat16).pin_memory()
+    groups = bs.group_descs([(dA[o:o + m], sa, b, sb, dC[o:o + m]) for o, m, sa, b, sb in
+                             zip(p.offsets, p.Ms, dsA, dB, dsB)])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dA.copy_(hA, non_blocking=True)
+        for d, h in zip(dsA, hsA):
+            d.copy_(h, non_blocking=True)
+        dMs.copy_(hMs, non_blocking=True)
+        bs.fp8_gemm_grouped(groups, dMs, p.N, p.K, stream=stream)
+        hC.copy_(dC, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = t0.elapsed_time(t1) / steps
+    h2d = hA.numel() + sum(4 * s.numel() for s in hsA) + 4 * hMs.numel()
+    d2h = 2 * hC.numel()
+    return {"value": round(p.algorithmic_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "how": "weights resident in HBM; per step the activation rows, their scales and the row "
+                   "counts host->device (pinned), one grouped launch through the public API with a "
+                   "prebuilt descriptor array, all outputs device->host"}
+
+
 def cpu_baseline_sample(name, seconds=15.0):
     """The oracle, as it is, on a bounded sample of the workload's outputs."""
     import numpy as np
@@ -409,6 +481,45 @@ def cpu_baseline_sample(name, seconds=15.0):
                       f"{spent:.1f} s, fp64 oracle on all host threads"}
 
 
+def oracle_timings():
+    """The oracle on the other workloads: c0, c1 and the grouped decode in
+    full on all host threads, the 8192^3 arbitrary-scale GEMM on its first
+    512 rows (all columns), and one thread on c0 in full and on the first 128
+    rows of c1.  Seconds and effective GFLOP/s of each run."""
+    import oracle
+    import workloads
+    cores = os.cpu_count() or 1
+    out = {}
+
+    def timed(key, fn, flops, threads, sample):
+        t0 = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t0
+        out[key] = {"seconds": round(dt, 3), "gflops": round(flops / dt / 1e9, 2), "threads": threads,
+                    "sample": sample}
+
+    for name in ("c0", "c1"):
+        p = workloads.make(name, seed=0, device="cpu")
+        A, sA, B, sB = (t.numpy() for t in (p.A, p.sA, p.B, p.sB))
+        timed(name, lambda: oracle.gemm(A, sA, B, sB, p.M, p.N, p.K, nthreads=cores), p.flops, cores,
+              f"full {p.M}x{p.N}x{p.K}")
+        rows = p.M if name == "c0" else 128
+        timed(f"{name}_1thread",
+              lambda: oracle.gemm(A[:rows], sA[:(rows + 31) // 32], B, sB, rows, p.N, p.K, nthreads=1),
+              2 * rows * p.N * p.K, 1, f"first {rows} rows x all {p.N} columns")
+    gp = workloads.make("c3", seed=0, device="cpu")
+    timed("c3", lambda: oracle.grouped([gp.A_group(g).numpy() for g in range(gp.G)],
+                                       [s.numpy() for s in gp.sA], [b.numpy() for b in gp.B],
+                                       [s.numpy() for s in gp.sB], gp.Ms, gp.N, gp.K, nthreads=cores),
+          gp.flops, cores, f"full: G={gp.G}, sum M_g={sum(gp.Ms)}, N={gp.N}, K={gp.K}")
+    p = workloads.make("c4", seed=0, device="cpu")
+    rows = 512
+    A, sA, B, sB = (t.numpy() for t in (p.A, p.sA, p.B, p.sB))
+    timed("c4", lambda: oracle.gemm(A[:rows], sA[:rows // 32], B, sB, rows, p.N, p.K, nthreads=cores),
+          2 * rows * p.N * p.K, cores, f"first {rows} rows x all {p.N} columns of {p.M}x{p.N}x{p.K}")
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -427,20 +538,28 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     results = {}
-    names = [HEADLINE] + ([] if args.headline_only else ["c2", "c3", "c4", "c4p", "q8", "r1", "f1"])
+    hashes = {}
+    names = [HEADLINE] + ([] if args.headline_only else ["c1", "c3", "c4", "c4p", "q8", "r1", "f1"])
     if args.only:
         names = [args.only]
+    launches = 0
     with ClockSampler(local) as clk:
         for name in names:
-            run, flops, nbytes = make_runner(name, dev, bs)
-            ms = time_device(run, args.steps, args.warmup, dev, flush, world, flush=name not in UNFLUSHED)
+            run, flops, nbytes, bufs = make_runner(name, dev, bs)
+            if not args.only and name != "c4p":
+                hashes[name] = {k: sha256_of(v) for k, v in bufs.items()}
+            ms = time_device(run, args.steps, args.warmup, dev, flush, world,
+                             flush=None if name in UNFLUSHED else "write")
+            launches += args.steps
             mean_ms = max_over_ranks(sum(ms) / len(ms), world)
             results[name] = {"ms": mean_ms, "flops": flops, "bytes": nbytes,
                              "ms_min": min(ms), "ms_median": statistics.median(ms)}
             if name in UNFLUSHED and not args.only:
-                msf = time_device(run, args.steps, args.warmup, dev, flush, world, flush=True)
-                results[name]["ms_flushed"] = max_over_ranks(sum(msf) / len(msf), world)
-            del run
+                for how in ("read", "write"):
+                    msf = time_device(run, args.steps, args.warmup, dev, flush, world, flush=how)
+                    launches += args.steps
+                    results[name][f"ms_{how}_flushed"] = max_over_ranks(sum(msf) / len(msf), world)
+            del run, bufs
             torch.cuda.empty_cache()
     status = bs.fp8_status_query()
     if status != 0:
@@ -452,9 +571,15 @@ def run_ours(args):
                               "tflops": r["flops"] / (r["ms"] * 1e-3) / 1e12,
                               "gbs": r["bytes"] / (r["ms"] * 1e-3) / 1e9}))
         return
-    e2e = time_e2e(HEADLINE, max(3, args.steps // 5), args.warmup, dev, bs, world)
-    graph_c3 = (time_graph_grouped(args.steps, args.warmup, dev, bs, flush)
-                if "c3" in names and world == 1 else None)
+    e2e_steps = max(3, args.steps // 5)
+    e2e = time_e2e(HEADLINE, e2e_steps, args.warmup, dev, bs, world)
+    launches += e2e_steps
+    graph_c3 = e2e_c3 = None
+    if "c3" in names and world == 1:
+        graph_c3 = time_graph_grouped(args.steps, args.warmup, dev, bs, flush)
+        launches += args.steps
+        e2e_c3 = time_e2e_grouped(e2e_steps, args.warmup, dev, bs, world)
+        launches += e2e_steps
 
     if rank != 0:
         return
@@ -471,6 +596,7 @@ def run_ours(args):
         ach = r["flops"] / (r["ms"] * 1e-3) / 1e12
         return {"bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1),
                 "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4),
+                "frac_of_nominal_4500": round(ach / 4500.0, 4),
                 "traffic": recorded_traffic(name),
                 "peak_source": f"{pk_src} bf16 burst x {FP8_PER_BF16} (nominal fp8/bf16 ratio)"}
 
@@ -485,12 +611,16 @@ def run_ours(args):
             entry["algorithmic_bytes"] = r["bytes"]
             if name == "c3" and graph_c3:
                 entry["graph_replay"] = graph_c3
+            if name == "c3" and e2e_c3:
+                entry["e2e"] = e2e_c3
             if name in UNFLUSHED:
                 entry["l2"] = "not flushed: the step's 470 MB of weights exceed the 129 MB L2"
-                if "ms_flushed" in r:
-                    entry["with_l2_write_flush"] = {
-                        "ms_per_step": round(r["ms_flushed"], 4),
-                        "value": round(r["bytes"] / (r["ms_flushed"] * 1e-3) / 1e9, 1), "unit": "GB/s"}
+                for how in ("read", "write"):
+                    k = f"ms_{how}_flushed"
+                    if k in r:
+                        entry[f"with_l2_{how}_flush"] = {
+                            "ms_per_step": round(r[k], 4),
+                            "value": round(r["bytes"] / (r[k] * 1e-3) / 1e9, 1), "unit": "GB/s"}
         else:
             entry["value"] = round(r["flops"] / (r["ms"] * 1e-3) / 1e12, 1)
             entry["unit"] = "TFLOP/s"
@@ -509,15 +639,16 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 accumulate -> bf16",
         "data": "synthetic (seeded; shapes and value distributions of the workloads)",
-        "config": {"workload": WORKLOAD_NAMES[HEADLINE], "M": 4096, "N": 4096, "K": 4096,
+        "config": {"workload": WORKLOAD_NAMES[HEADLINE], **HEADLINE_SHAPE,
                    "l2": "flushed between timed steps (512 MiB write)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline(HEADLINE),
         # launches of this library's kernels inside timed regions: every timed
-        # step of every workload, the graph replays and the end-to-end steps
-        "gpu_launches": (args.steps * (len(names) + sum(n in UNFLUSHED for n in names))
-                         + (args.steps if graph_c3 else 0) + max(3, args.steps // 5)),
+        # step of every workload (the grouped decode three times: unflushed,
+        # read- and write-flushed), its graph replays and the end-to-end steps
+        "gpu_launches": launches,
         "clocks": clk.summary(),
+        "inputs": {"torch": torch.__version__, "sha256": hashes},
         "extra": extra,
     }
     if e2e:
@@ -529,6 +660,7 @@ def run_ours(args):
                               "device->host; steps pipelined over 3 streams, device buffers doubled"}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(HEADLINE, seconds=args.cpu_seconds)
+        line["cpu_baseline"]["other_workloads"] = oracle_timings()
     print(json.dumps(line))
 
 
@@ -568,7 +700,9 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": {"workload": WORKLOAD_NAMES[HEADLINE], "M": 4096, "N": 4096, "K": 4096},
+        "config": {"workload": WORKLOAD_NAMES[HEADLINE], **HEADLINE_SHAPE,
+                   "l2": "flushed between timed steps (512 MiB write)",
+                   "parallelism": f"replicas x{world}"},
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

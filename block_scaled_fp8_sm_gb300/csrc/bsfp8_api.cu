@@ -106,7 +106,11 @@ int device_setup(DeviceState **out) {
     if (rc != FP8_OK) return rc;
     if (!d.status) {
         if (cudaMalloc(&d.status, 256) != cudaSuccess) return FP8_ERR_CUDA;
-        if (cudaMemset(d.status, 0, 256) != cudaSuccess) return FP8_ERR_CUDA;
+        // the clear lands before any kernel of a later call, whatever stream
+        // that call uses (a memset on the legacy stream is not ordered with a
+        // non-blocking stream's work)
+        if (cudaMemset(d.status, 0, 256) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+            return FP8_ERR_CUDA;
     }
     d.sm_count = sms;
     d.ready = true;
@@ -404,8 +408,10 @@ int noalloc_setup(NoAllocState **out) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
         return FP8_ERR_CUDA;
-    // the status word must start at zero; later calls only OR bits into it
-    if (cudaMemset(p, 0, sizeof(uint32_t) * kNoAllocScratchWords) != cudaSuccess)
+    // the status word must start at zero (later calls only OR bits into it),
+    // and the clear must land before the first kernel, on whatever stream
+    if (cudaMemset(p, 0, sizeof(uint32_t) * kNoAllocScratchWords) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
         return FP8_ERR_CUDA;
     st.scratch = static_cast<uint32_t *>(p);
     st.sm_count = sms;
@@ -435,7 +441,7 @@ int launch_plain_noalloc(const void *A, const float *sA, const void *B, const fl
     {
         std::lock_guard<std::mutex> lk(g_mu);
         c.wait_limit = wait_limit_locked();
-        c.withhold_stage = -1;
+        c.withhold_stage = g_withhold_stage;   // debug control, -1 unless a test sets it
         c.trace = nullptr;
     }
     int rc = encode_kmajor(&args.tmA, A, M, K, BM);
@@ -451,6 +457,18 @@ int launch_plain_noalloc(const void *A, const float *sA, const void *B, const fl
     const int grid = c.num_tiles < st->sm_count ? c.num_tiles : st->sm_count;
     bsfp8_gemm_plain<BN><<<grid, NUM_THREADS, smem_bytes<BN>(), stream>>>(args);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+// Reads and clears one device status word: `stream` has been synchronised;
+// the clear is ordered on `stream` and waited for.
+int read_and_clear(uint32_t *word_dev, uint32_t *word, cudaStream_t stream) {
+    *word = 0;
+    if (!word_dev) return FP8_OK;
+    if (cudaMemcpy(word, word_dev, sizeof *word, cudaMemcpyDeviceToHost) != cudaSuccess) return FP8_ERR_CUDA;
+    if (*word != 0 && (cudaMemsetAsync(word_dev, 0, sizeof *word, stream) != cudaSuccess ||
+                       cudaStreamSynchronize(stream) != cudaSuccess))
+        return FP8_ERR_CUDA;
+    return FP8_OK;
 }
 
 }  // namespace
@@ -594,14 +612,24 @@ int fp8_gemm_grouped(const fp8_group_desc *groups, const int32_t *Ms, int64_t N,
 
 int fp8_status_query(cudaStream_t stream, int *status) {
     if (!status) return FP8_ERR_NULL;
-    DeviceState *d = nullptr;
-    int rc = device_setup(&d);
-    if (rc != FP8_OK) return rc;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return FP8_ERR_CUDA;
+    // the words of whichever entry points have run on this device (the
+    // regular status word and word 0 of the allocation-free scratch array);
+    // nothing is set up or allocated here
+    uint32_t *regular = nullptr, *noalloc = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_dev[dev].ready) regular = g_dev[dev].status;
+        if (g_noalloc[dev].ready) noalloc = g_noalloc[dev].scratch;
+    }
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8_ERR_CUDA;
-    uint32_t word = 0;
-    if (cudaMemcpy(&word, d->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
-        return FP8_ERR_CUDA;
-    if (word != 0 && cudaMemset(d->status, 0, sizeof word) != cudaSuccess) return FP8_ERR_CUDA;
+    uint32_t w1 = 0, w2 = 0;
+    int rc = read_and_clear(regular, &w1, stream);
+    if (rc != FP8_OK) return rc;
+    rc = read_and_clear(noalloc, &w2, stream);
+    if (rc != FP8_OK) return rc;
+    const uint32_t word = w1 | w2;
     *status = (word & STATUS_TIMEOUT) ? FP8_ERR_TIMEOUT : (word & STATUS_SCALE) ? FP8_ERR_SCALE : FP8_OK;
     return FP8_OK;
 }
@@ -646,6 +674,9 @@ int fp8_quantize_blocks(const void *x, void *q, float *s, int64_t M, int64_t K, 
     if (M == 0 || K == 0) return FP8_OK;
     if (!x || !q || !s) return FP8_ERR_NULL;
     if (!aligned(x, 16) || !aligned(q, 16) || !aligned(s, 4)) return FP8_ERR_ALIGN;
+    DeviceState *d = nullptr;
+    const int rc = device_setup(&d);   // architecture check (sm_103 only)
+    if (rc != FP8_OK) return rc;
     const int64_t MB = (M + 31) / 32;
     const dim3 grid(static_cast<unsigned>((K + QT_COLS - 1) / QT_COLS),
                     static_cast<unsigned>(MB < 65535 ? MB : 65535));
@@ -665,6 +696,9 @@ void fp8_lib_shutdown(void) {
             }
         }
         g_dev[i] = DeviceState();
+        // the allocation-free entry point's static array stays (it belongs to
+        // the loaded module); its set-up runs again on the next call
+        g_noalloc[i] = NoAllocState();
     }
     std::lock_guard<std::mutex> lm(g_map_mu);
     g_maps.clear();

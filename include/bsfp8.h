@@ -16,7 +16,8 @@
  * aif.amtbbs.org post 29992, section 1: a row's result changes with the batch
  * only through the reduction split).  Hence every output row is bit-identical
  * whatever M (and whatever other rows) it is computed with, given the same
- * path (see FP8_PATH_*).
+ * path; FP8_PATH_* below says when AUTO's choice of path can itself depend on
+ * other rows, and FP8_PATH_PROMOTE is batch-invariant for any scales.
  *
  * Layouts (all device memory, all row-major, caller-owned):
  *   A   [M, K]           E4M3 codes, one byte each (row stride K bytes)
@@ -70,15 +71,24 @@ enum {
  *   taken when every scale the tile reads (its row blocks of sA and column
  *   blocks of sB, all of K) is a positive normal power of two; otherwise the
  *   promotion path.  A row's bits therefore depend only on the scales of the
- *   rows in its own 256-row tile (rows 256*floor(m/256) ...).
+ *   rows in its own 256-row tile (rows 256*floor(m/256) ...), and only when
+ *   sA's 32-row blocks mix kinds: AUTO is batch-invariant (a row gets the same
+ *   bits for every M) whenever every row block of sA is of one kind -- all of
+ *   its K/32 scales powers of two in every block, or at least one scale that
+ *   is not in every block -- whatever sB holds (every launch reads the same
+ *   sB).  Where sA's row blocks do mix, a row computed with fewer rows (M
+ *   ending inside its tile) may take the native path while the full batch
+ *   promotes the tile; its bits are then those of one of the two pinned paths
+ *   below.  Callers that need batch invariance for any scales pin
+ *   FP8_PATH_PROMOTE.
  * FP8_PATH_NATIVE: block-scaled tensor-core path (kind::mxf8f6f4 with UE8M0
  *   scales, exact for power-of-two scales).  A tile that finds another scale
  *   is computed by the promotion path and FP8_ERR_SCALE is recorded.
  * FP8_PATH_PROMOTE: per-K-block fp32 promotion for arbitrary fp32 scales:
  *   unscaled 32-deep tensor-core partials, scaled and accumulated in fp32.
- *   Runs on single-CTA 128 x 256 tiles (faster for this path than CTA
- *   pairs); each element equals, bit for bit, what AUTO computes for it on a
- *   promoted tile. */
+ *   Every tile takes this path whatever the scales, so each row's bits are
+ *   the same for every M (batch-invariant unconditionally); each element
+ *   equals, bit for bit, what AUTO computes for it on a promoted tile. */
 enum { FP8_PATH_AUTO = 0, FP8_PATH_NATIVE = 1, FP8_PATH_PROMOTE = 2 };
 
 /* Block-scaled GEMM, AUTO path.  Returns FP8_OK or FP8_ERR_*.
@@ -136,8 +146,14 @@ int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *
  * FP8_ERR_CUDA (launch failure). */
 int fp8_quantize_blocks(const void *x, void *q, float *s, int64_t M, int64_t K, cudaStream_t stream);
 
-/* Allocation-free variant of fp8_gemm_blockscaled (AUTO path, same layouts,
- * constraints and results).  The pages have no counterpart: this entry point
+/* Allocation-free variant of fp8_gemm_blockscaled (AUTO path, same layouts
+ * and constraints).  It runs one CTA per 128 x 256 tile instead of CTA pairs
+ * on 256 x 256 tiles, with the same per-element arithmetic: its output equals
+ * fp8_gemm_blockscaled's bit for bit whenever both choose the same path for
+ * every element, which holds when sA's row blocks are all of one kind (see
+ * FP8_PATH_AUTO).  Where sA's row blocks mix kinds, AUTO's 128-row and
+ * 256-row tiles can choose differently; both results are then within the
+ * same tolerance of the exact value.  The pages have no counterpart: this entry point
  * exists for callers that cannot allocate device memory: an inference server
  * whose caching allocator owns the whole device (a stray cudaMalloc there can
  * fail, fragment the pool or stall the device while it synchronises), or a
@@ -151,8 +167,9 @@ int fp8_quantize_blocks(const void *x, void *q, float *s, int64_t M, int64_t K, 
  * (looks up the array's device address and clears it); make that first call
  * before any stream capture.  All calls share the array: calls that overlap
  * on the GPU race on it (only their status bits mix; results are not
- * affected).  Device-side conditions of these calls (a wait that ran out) go
- * to that array, not to the word fp8_status_query reads. */
+ * affected).  Device-side conditions of these calls (a wait that ran out)
+ * are recorded in word 0 of that array; fp8_status_query reads and clears it
+ * together with the regular status word, and allocates nothing either. */
 #define FP8_NOALLOC_SCRATCH_BYTES 256
 int fp8_gemm_blockscaled_noalloc(const void *A, const float *sA, const void *B, const float *sB,
                                  void *C, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
@@ -183,7 +200,9 @@ typedef struct fp8_group_desc {
  * Groups are independent GEMMs: group g's result is bit-identical to
  * fp8_gemm_blockscaled on that group alone with the same path.
  * G <= FP8_MAX_GROUPS_PER_LAUNCH runs as one launch; larger G is split into
- * consecutive launches of at most that many groups on the same stream. */
+ * consecutive launches of at most that many groups on the same stream.
+ * K = 0 returns FP8_ERR_SHAPE (the row counts live on the device, so the
+ * host cannot zero-fill the outputs); G = 0 or N = 0 enqueues nothing. */
 int fp8_gemm_grouped(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, int64_t K,
                      int32_t G, cudaStream_t stream);
 
@@ -191,9 +210,13 @@ int fp8_gemm_grouped_ex(const fp8_group_desc *groups, const int32_t *Ms, int64_t
                         int64_t K, int32_t G, int mode, cudaStream_t stream);
 
 /* Synchronises `stream`, then reads and clears the current device's status
- * word.  *status = FP8_OK, or the FP8_ERR_* code of the condition recorded
- * first since the last query (FP8_ERR_TIMEOUT takes precedence).  Returns
- * FP8_OK or FP8_ERR_CUDA / FP8_ERR_NULL. */
+ * words: the one the regular entry points write and word 0 of the
+ * allocation-free entry point's static array (each only once its entry point
+ * has run on this device).  Allocates nothing.  *status = FP8_OK, or the
+ * FP8_ERR_* code of a condition recorded since the last query
+ * (FP8_ERR_TIMEOUT takes precedence over FP8_ERR_SCALE).  The status comes
+ * back through the out-pointer so that the return value stays the call's own
+ * FP8_OK / FP8_ERR_CUDA / FP8_ERR_NULL. */
 int fp8_status_query(cudaStream_t stream, int *status);
 
 /* Human-readable name of an FP8_* code (static storage). */
@@ -222,7 +245,11 @@ int fp8_debug_set(int key, int64_t value);
 
 /* Frees the per-device status words and empties the host cache of TMA
  * descriptors (each is a pure function of a call's pointers and sizes, so the
- * cache never holds a stale one).  Later calls set both up again. */
+ * cache never holds a stale one).  Later calls set both up again.  The
+ * allocation-free entry point's static array is part of the loaded library
+ * and stays; its per-device set-up (the array's device address, kernel
+ * attributes) is forgotten and runs again on that entry point's next call,
+ * which must then again come before any stream capture. */
 void fp8_lib_shutdown(void);
 
 #ifdef __cplusplus
