@@ -280,7 +280,7 @@ def time_device(run, steps, warmup, dev, flush_buf, world, flush="write"):
         if flush == "write":
             flush_buf.fill_(i & 0xFF)      # evict the operands from L2
         elif flush == "read":
-            torch.sum(flush_buf.view(torch.int64), out=sink)
+            torch.sum(flush_buf.view(torch.int64), dim=(0,), out=sink)
         ev[i][0].record(stream)
         run(stream)
         ev[i][1].record(stream)
