@@ -1245,9 +1245,26 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                             // (a pair's peer: its MMA warp forwards the release)
                             if (lane == 0) mbar_arrive(&ctl->tempty[b]);
                         }
+                        if constexpr (PAIR) {
 #pragma unroll
-                        for (int y = 0; y < 16; ++y)
-                            acc[16 * x + y] = fmaf(sc[x >> 1], __uint_as_float(r[y]), acc[16 * x + y]);
+                            for (int y = 0; y < 16; ++y)
+                                acc[16 * x + y] = fmaf(sc[x >> 1], __uint_as_float(r[y]), acc[16 * x + y]);
+                        } else {
+                            // single-CTA tiles: packed two-lane FMAs (the same fma per
+                            // element, half the issue slots; measured 6 % faster here,
+                            // not on CTA pairs)
+                            const uint64_t s2 = f32x2_pack(__float_as_uint(sc[x >> 1]), __float_as_uint(sc[x >> 1]));
+#pragma unroll
+                            for (int y = 0; y < 8; ++y) {
+                                uint64_t a2 = f32x2_pack(__float_as_uint(acc[16 * x + 2 * y]),
+                                                         __float_as_uint(acc[16 * x + 2 * y + 1]));
+                                fma_f32x2(a2, s2, f32x2_pack(r[2 * y], r[2 * y + 1]));
+                                uint32_t lo, hi;
+                                f32x2_unpack(a2, lo, hi);
+                                acc[16 * x + 2 * y] = __uint_as_float(lo);
+                                acc[16 * x + 2 * y + 1] = __uint_as_float(hi);
+                            }
+                        }
                     }
                     if (b) ++uses1; else ++uses0;
                     ++pk;

@@ -276,6 +276,22 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------ fp32 pairs ----
+// Two fp32 values in one 64-bit register pair (low word = first value).
+__device__ __forceinline__ uint64_t f32x2_pack(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, uint32_t &lo, uint32_t &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+// acc = a * b + acc on both halves, each an fp32 fma rounded to nearest even
+// (the packed form issues one instruction for two lanes of work).
+__device__ __forceinline__ void fma_f32x2(uint64_t &acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
 // ----------------------------------------------------------- descriptors ----
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
 // layout: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked along
