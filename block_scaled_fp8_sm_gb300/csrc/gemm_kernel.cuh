@@ -514,7 +514,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0u;
     const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int grid_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     const int row_off = static_cast<int>(rank) * BM;
 
     if (threadIdx.x == 0) {
@@ -592,7 +592,18 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 
     const uint32_t tmem = ctl->tmem_base;
     const int num_tiles = ctl->num_tiles;
-    const int my_tiles = (unit < num_tiles) ? (num_tiles - unit + nunits - 1) / nunits : 0;
+    // Grouped launches use only as many CTAs as give each the same number of
+    // tiles (the tile count is known here, from the device row counts): every
+    // CTA streams its weights at a rate bounded by the bytes it holds in
+    // flight, so a last round with fewer CTAs would run below the memory's
+    // bandwidth (16 groups of 4096 x 7168 weights, 256 tiles: 128 CTAs with
+    // two each take 90 us, 152 CTAs of which 104 take a second tile 93 us).
+    int nunits = grid_units;
+    if constexpr (GROUPED) {
+        const int rounds = (num_tiles + grid_units - 1) / grid_units;
+        nunits = rounds > 0 ? (num_tiles + rounds - 1) / rounds : grid_units;
+    }
+    const int my_tiles = (unit < num_tiles && unit < nunits) ? (num_tiles - unit + nunits - 1) / nunits : 0;
     GroupEntry e0{};
     if constexpr (!GROUPED) e0 = args.e;
     const Sched<BN, GROUPED, Args, C::TILE_M> sch{args, c, ctl->tile_start, ctl->mg, e0};
