@@ -16,6 +16,7 @@ from ._abi import (FP8_PATH_AUTO, FP8_PATH_NATIVE, FP8_PATH_PROMOTE,  # noqa: F4
                    FP8_MAX_GROUPS_PER_LAUNCH, fp8_group_desc)
 
 __all__ = ["fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_gemm_grouped", "group_descs",
+           "fp8_gemm_grouped_device", "fp8_grouped_workspace_bytes", "group_table",
            "fp8_quantize_blocks", "fp8_gemm_rowcol", "fp8_gemm_blockscaled_residual",
            "fp8_status_query", "fp8_strerror", "fp8_version", "fp8_debug_set", "fp8_lib_shutdown",
            "Fp8Error", "library"]
@@ -157,6 +158,32 @@ def fp8_gemm_grouped(groups, Ms, N, K, G=None, stream=None, mode=None):
     else:
         rc = lib.fp8_gemm_grouped_ex(arr, ms, N, K, G, int(mode), s)
     _check(rc, "fp8_gemm_grouped")
+
+
+def group_table(groups, device):
+    """The records of fp8_gemm_grouped_device: an int64 CUDA tensor [G, 5]
+    holding each group's (A, sA, B, sB, C) device pointers, in the layout of
+    fp8_group_desc.  The tensors must stay alive while launches use it."""
+    import torch
+    rows = [[x if isinstance(x, int) else _ptr(x) for x in g] for g in groups]
+    return torch.tensor(rows, dtype=torch.int64).reshape(len(rows), 5).to(device)
+
+
+def fp8_grouped_workspace_bytes(G: int) -> int:
+    return library().fp8_grouped_workspace_bytes(int(G))
+
+
+def fp8_gemm_grouped_device(table, Ms, N, K, workspace, G=None, stream=None):
+    """Grouped GEMM whose records live in device memory: ``table`` is an
+    int64 CUDA tensor [G, 5] of device pointers (see group_table), ``Ms`` an
+    int32 CUDA tensor of row counts, ``workspace`` a CUDA tensor of at least
+    fp8_grouped_workspace_bytes(G) bytes (128-byte aligned).  Every argument
+    stays on the device, so a CUDA graph captured once follows later changes
+    of the table and the row counts."""
+    G = table.shape[0] if G is None else G
+    rc = library().fp8_gemm_grouped_device(_ptr(table), _ptr(Ms), N, K, G, _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "fp8_gemm_grouped_device")
 
 
 def fp8_status_query(stream=None) -> int:

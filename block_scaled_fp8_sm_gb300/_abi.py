@@ -20,6 +20,7 @@ FP8_ERR_CUDA = -5
 FP8_ERR_MODE = -6
 FP8_ERR_SCALE = -7
 FP8_ERR_TIMEOUT = -8
+FP8_ERR_RECORD = -9
 
 FP8_PATH_AUTO = 0
 FP8_PATH_NATIVE = 1
@@ -37,6 +38,7 @@ EXPORTS = (
     "fp8_gemm_grouped_ex", "fp8_status_query", "fp8_strerror", "fp8_version",
     "fp8_debug_set", "fp8_lib_shutdown", "fp8_gemm_blockscaled_noalloc",
     "fp8_quantize_blocks", "fp8_gemm_rowcol", "fp8_gemm_blockscaled_residual",
+    "fp8_gemm_grouped_device", "fp8_grouped_workspace_bytes",
 )
 
 
@@ -75,6 +77,10 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fp8_gemm_grouped.restype = ci
     lib.fp8_gemm_grouped_ex.argtypes = [ctypes.POINTER(fp8_group_desc), vp, i64, i64, i32, ci, vp]
     lib.fp8_gemm_grouped_ex.restype = ci
+    lib.fp8_gemm_grouped_device.argtypes = [vp, vp, i64, i64, i32, vp, i64, vp]
+    lib.fp8_gemm_grouped_device.restype = ci
+    lib.fp8_grouped_workspace_bytes.argtypes = [i32]
+    lib.fp8_grouped_workspace_bytes.restype = i64
     lib.fp8_status_query.argtypes = [vp, ctypes.POINTER(ci)]
     lib.fp8_status_query.restype = ci
     lib.fp8_strerror.argtypes = [ci]

@@ -59,6 +59,9 @@ int set_kernel_attrs() {
     if (cudaFuncSetAttribute(bsfp8_gemm_grouped<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN, false, true>()) != cudaSuccess)
         return FP8_ERR_CUDA;
+    if (cudaFuncSetAttribute(bsfp8_gemm_grouped_dev<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<BN, false, true>()) != cudaSuccess)
+        return FP8_ERR_CUDA;
     if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN, true>()) != cudaSuccess)
         return FP8_ERR_CUDA;
@@ -353,6 +356,35 @@ int launch_grouped(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, i
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
+// Grouped launch with device-resident records: the prepare kernel builds the
+// groups' B tensor maps in the workspace, the GEMM kernel reads maps and
+// records from device memory.  Both are ordinary launches on `stream`, so a
+// captured graph replays them with whatever the table holds at that time.
+constexpr int64_t kMapBytes = 128;
+int64_t grouped_ws_bytes(int32_t G) { return static_cast<int64_t>(G) * (kMapBytes + 4) + 256; }
+
+template <int BN>
+int launch_grouped_dev(const GroupRecord *table, const int32_t *Ms, int64_t N, int64_t K, int32_t G,
+                       CUtensorMap *maps, int32_t *valid, int mode, DeviceState *d, cudaStream_t stream) {
+    // the template: shape N x K, box of BN rows; its base (here the map slots'
+    // own address, any valid one will do) is replaced per group on the device
+    CUtensorMap tmpl;
+    int rc = encode_kmajor(&tmpl, maps, N, K, BN);
+    if (rc != FP8_OK) return rc;
+    bsfp8_grouped_prepare<<<(G + 3) / 4, 128, 0, stream>>>(tmpl, table, G, maps, valid, d->status);
+    if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
+    GroupedDevArgs args;
+    std::memset(&args, 0, sizeof args);
+    fill_common(args.c, 0, N, K, mode, d, BN);
+    args.c.G = G;
+    args.c.Ms = Ms;
+    args.table = table;
+    args.maps = maps;
+    args.valid = valid;
+    bsfp8_gemm_grouped_dev<BN><<<d->sm_count, NUM_THREADS, smem_bytes<BN, false, true>(), stream>>>(args);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
 // ------------------------------------------- allocation-free entry point ----
 // fp8_gemm_blockscaled_noalloc runs the same kernel, but the device status
 // word it needs lives in this file-scope array instead of memory obtained from
@@ -610,6 +642,33 @@ int fp8_gemm_grouped(const fp8_group_desc *groups, const int32_t *Ms, int64_t N,
     return fp8_gemm_grouped_ex(groups, Ms, N, K, G, FP8_PATH_AUTO, stream);
 }
 
+int64_t fp8_grouped_workspace_bytes(int32_t G) { return G < 0 ? 0 : grouped_ws_bytes(G); }
+
+int fp8_gemm_grouped_device(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, int64_t K, int32_t G,
+                            void *workspace, int64_t workspace_bytes, cudaStream_t stream) {
+    static_assert(sizeof(fp8_group_desc) == sizeof(GroupRecord), "record layout");
+    int rc = check_shape(0, N, K);
+    if (rc != FP8_OK) return rc;
+    if (G < 0) return FP8_ERR_SHAPE;
+    if (G == 0 || N == 0) return FP8_OK;
+    if (!groups || !Ms || !workspace) return FP8_ERR_NULL;
+    if (!aligned(groups, 8) || !aligned(Ms, 4) || !aligned(workspace, 128)) return FP8_ERR_ALIGN;
+    if (workspace_bytes < grouped_ws_bytes(G)) return FP8_ERR_SHAPE;
+    DeviceState *d = nullptr;
+    rc = device_setup(&d);
+    if (rc != FP8_OK) return rc;
+    if (K == 0) return FP8_ERR_SHAPE;   // as fp8_gemm_grouped: no host-side zero fill
+    CUtensorMap *maps = static_cast<CUtensorMap *>(workspace);
+    int32_t *valid = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) + static_cast<int64_t>(G) * kMapBytes);
+    const GroupRecord *table = reinterpret_cast<const GroupRecord *>(groups);
+    for (int32_t g0 = 0; g0 < G; g0 += FP8_MAX_GROUPS_PER_LAUNCH) {
+        const int32_t n = (G - g0) < FP8_MAX_GROUPS_PER_LAUNCH ? (G - g0) : FP8_MAX_GROUPS_PER_LAUNCH;
+        rc = launch_grouped_dev<TILE_N>(table + g0, Ms + g0, N, K, n, maps + g0, valid + g0, FP8_PATH_AUTO, d, stream);
+        if (rc != FP8_OK) return rc;
+    }
+    return FP8_OK;
+}
+
 int fp8_status_query(cudaStream_t stream, int *status) {
     if (!status) return FP8_ERR_NULL;
     int dev = 0;
@@ -630,7 +689,10 @@ int fp8_status_query(cudaStream_t stream, int *status) {
     rc = read_and_clear(noalloc, &w2, stream);
     if (rc != FP8_OK) return rc;
     const uint32_t word = w1 | w2;
-    *status = (word & STATUS_TIMEOUT) ? FP8_ERR_TIMEOUT : (word & STATUS_SCALE) ? FP8_ERR_SCALE : FP8_OK;
+    *status = (word & STATUS_TIMEOUT)  ? FP8_ERR_TIMEOUT
+              : (word & STATUS_RECORD) ? FP8_ERR_RECORD
+              : (word & STATUS_SCALE)  ? FP8_ERR_SCALE
+                                       : FP8_OK;
     return FP8_OK;
 }
 
@@ -645,6 +707,7 @@ const char *fp8_strerror(int code) {
         case FP8_ERR_MODE: return "FP8_ERR_MODE: unknown path mode or debug key";
         case FP8_ERR_SCALE: return "FP8_ERR_SCALE: native path forced with a scale that is not a power of two";
         case FP8_ERR_TIMEOUT: return "FP8_ERR_TIMEOUT: a device-side wait ran out";
+        case FP8_ERR_RECORD: return "FP8_ERR_RECORD: a device-resident group record held a null or misaligned pointer (group skipped)";
         default: return "unknown FP8 status code";
     }
 }

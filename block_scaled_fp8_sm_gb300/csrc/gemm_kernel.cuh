@@ -88,7 +88,7 @@ constexpr int MAX_GROUPS = 64;
 constexpr int GROUP_M = 8;         // tile-order swizzle width (m-tiles) for L2 reuse
 constexpr int TILE_N = 256;        // the BN every launch uses
 
-enum : uint32_t { STATUS_TIMEOUT = 1u, STATUS_SCALE = 2u };
+enum : uint32_t { STATUS_TIMEOUT = 1u, STATUS_SCALE = 2u, STATUS_RECORD = 4u };
 enum : int { PATH_AUTO = 0, PATH_NATIVE = 1, PATH_PROMOTE = 2 };
 // Scale layouts (a kernel template parameter, so each layout compiles its own
 // kernel and the block-scaled kernels carry no code for the others):
@@ -212,6 +212,38 @@ struct GroupedArgs {
     GroupEntry e[MAX_GROUPS];
     Common c;
 };
+
+// One group's record in device memory (the C ABI's fp8_group_desc layout).
+struct GroupRecord {
+    const uint8_t *A;
+    const float *sA;
+    const uint8_t *B;
+    const float *sB;
+    __nv_bfloat16 *C;
+};
+
+// Grouped problems whose records live in device memory: the group table may
+// change between launches (or CUDA-graph replays) without the host.  The B
+// tensor maps are built on the device from a template by
+// bsfp8_grouped_prepare, which also checks each record.
+struct GroupedDevArgs {
+    const GroupRecord *table;   // [G] records
+    const CUtensorMap *maps;    // [G] B tensor maps (written by the prepare kernel)
+    const int32_t *valid;       // [G] 1: the record passed the checks; 0: the group is skipped
+    Common c;
+};
+
+__device__ __forceinline__ GroupEntry group_entry(const GroupedArgs &a, int g) { return a.e[g]; }
+__device__ __forceinline__ GroupEntry group_entry(const GroupedDevArgs &a, int g) {
+    const GroupRecord r = a.table[g];
+    return GroupEntry{r.A, r.sA, r.sB, r.C};
+}
+__device__ __forceinline__ const CUtensorMap *group_bmap(const GroupedArgs &a, int g) { return &a.tmB[g]; }
+__device__ __forceinline__ const CUtensorMap *group_bmap(const GroupedDevArgs &a, int g) { return a.maps + g; }
+__device__ __forceinline__ bool group_valid(const GroupedArgs &, int) { return true; }
+__device__ __forceinline__ bool group_valid(const GroupedDevArgs &a, int g) { return a.valid[g] != 0; }
+template <typename Args> struct DevTable { static constexpr bool value = false; };
+template <> struct DevTable<GroupedDevArgs> { static constexpr bool value = true; };
 
 template <int STAGES, int SF_STAGES>
 struct Ctrl {
@@ -373,7 +405,7 @@ struct Sched {
 
     __device__ __forceinline__ GroupEntry entry(int g) const {
         if constexpr (!GROUPED) return e0;
-        else return a.e[g];
+        else return group_entry(a, g);
     }
 };
 
@@ -558,7 +590,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             if (lane == 0) {
                 int acc = 0;
                 for (int g = 0; g < c.G; ++g) {
-                    int m = c.Ms[g];
+                    int m = group_valid(args, g) ? c.Ms[g] : 0;   // a rejected record: no rows
                     m = m < 0 ? 0 : m;
                     ctl->mg[g] = m;
                     ctl->tile_start[g] = acc;
@@ -582,7 +614,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 }
             }
         } else {
-            for (int g = lane; g < c.G; g += 32) tma_prefetch_desc(&args.tmB[g]);
+            if constexpr (!DevTable<Args>::value)
+                for (int g = lane; g < c.G; g += 32) tma_prefetch_desc(group_bmap(args, g));
         }
     }
     tc_fence_before();
@@ -639,8 +672,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             const Tile tt = sch.tile(unit + i * nunits);
             const GroupEntry e = sch.entry(tt.g);
             const CUtensorMap *tmb;
-            if constexpr (GROUPED) tmb = &args.tmB[tt.g];
+            if constexpr (GROUPED) tmb = group_bmap(args, tt.g);
             else tmb = &args.tmB;
+            // a map written on the device: its writes are acquired before use
+            if constexpr (DevTable<Args>::value) if (lane == 0) tensormap_acquire(tmb);
             const int a_rows = min(C::TILE_M, tt.Mg - tt.m0);   // grouped: A rows loaded by cp.async
             const uint8_t *a_base = e.A + static_cast<int64_t>(tt.m0) * c.K;
             for (int ks = 0, k0 = 0; ks < KW; ++ks, k0 += C::HALVES * BK) {
@@ -1344,6 +1379,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
 template <int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) bsfp8_gemm_grouped(const __grid_constant__ GroupedArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    gemm_body<BN, true, false>(args, smem_raw);
+}
+
+// Grouped problems with device-resident records (one warp per group): checks
+// the record (no null pointer; A, B, C 16-byte and sA, sB 4-byte aligned),
+// writes the group's B tensor map -- the host-encoded template (shape N x K,
+// box of BN rows) with the record's B as its base -- into maps[g], and
+// valid[g].  A rejected record sets STATUS_RECORD; its group is skipped.
+__global__ void __launch_bounds__(128) bsfp8_grouped_prepare(const __grid_constant__ CUtensorMap tmpl,
+                                                            const GroupRecord *table, int G, CUtensorMap *maps,
+                                                            int32_t *valid, uint32_t *status) {
+    __shared__ alignas(128) CUtensorMap sm_map[4];
+    const int w = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+    const int g = static_cast<int>(blockIdx.x) * 4 + w;
+    if (g >= G) return;   // the whole warp
+    if (lane < 8) reinterpret_cast<uint4 *>(&sm_map[w])[lane] = reinterpret_cast<const uint4 *>(&tmpl)[lane];
+    const GroupRecord r = table[g];
+    const auto al = [](const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+    const bool ok = r.A && r.sA && r.B && r.sB && r.C && al(r.A, 16) && al(r.B, 16) && al(r.C, 16) &&
+                    al(r.sA, 4) && al(r.sB, 4);
+    __syncwarp();
+    if (ok) {
+        if (lane == 0) tensormap_set_base_smem(smem_u32(&sm_map[w]), reinterpret_cast<uint64_t>(r.B));
+        __syncwarp();
+        tensormap_publish(&maps[g], smem_u32(&sm_map[w]));
+    }
+    if (lane == 0) {
+        valid[g] = ok ? 1 : 0;
+        if (!ok) atomicOr(status, STATUS_RECORD);
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1) bsfp8_gemm_grouped_dev(const __grid_constant__ GroupedDevArgs args) {
     extern __shared__ uint8_t smem_raw[];
     gemm_body<BN, true, false>(args, smem_raw);
 }

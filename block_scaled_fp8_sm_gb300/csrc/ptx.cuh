@@ -149,6 +149,26 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 // all committed bulk stores have completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// ------------------------------------------------- tensor maps on the device ----
+// Replace the global base address of a tensor map held in shared memory.
+__device__ __forceinline__ void tensormap_set_base_smem(uint32_t smem_map, uint64_t base) {
+    asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(smem_map), "l"(base)
+                 : "memory");
+}
+// Warp-wide: copy a 128-byte tensor map from shared to global memory and make
+// it visible to later tensor-map reads (release at GPU scope).
+__device__ __forceinline__ void tensormap_publish(void *gmem_map, uint32_t smem_map) {
+    asm volatile("tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned [%0], [%1], 128;" ::"l"(
+                     reinterpret_cast<uint64_t>(gmem_map)),
+                 "r"(smem_map)
+                 : "memory");
+}
+// Before a TMA uses a tensor map that was written in global memory.
+__device__ __forceinline__ void tensormap_acquire(const void *gmem_map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(gmem_map))
+                 : "memory");
+}
+
 // Named barrier over `count` threads (warp multiples).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

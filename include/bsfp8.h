@@ -63,7 +63,8 @@ enum {
     FP8_ERR_CUDA = -5,       /* a CUDA runtime/driver call failed (launch, attribute, ...) */
     FP8_ERR_MODE = -6,       /* unknown path mode or debug key */
     FP8_ERR_SCALE = -7,      /* device status: FP8_PATH_NATIVE with a scale that is not 2^e */
-    FP8_ERR_TIMEOUT = -8     /* device status: a bounded wait inside a kernel ran out */
+    FP8_ERR_TIMEOUT = -8,    /* device status: a bounded wait inside a kernel ran out */
+    FP8_ERR_RECORD = -9      /* device status: a device-resident group record was rejected */
 };
 
 /* Path selection.
@@ -209,12 +210,43 @@ int fp8_gemm_grouped(const fp8_group_desc *groups, const int32_t *Ms, int64_t N,
 int fp8_gemm_grouped_ex(const fp8_group_desc *groups, const int32_t *Ms, int64_t N,
                         int64_t K, int32_t G, int mode, cudaStream_t stream);
 
+/* Grouped GEMM with the group records in DEVICE memory (FP8 GEMM library
+ * article, hncyxsy.com/news/241433, section 4.2: the grouped kernel finds its
+ * problems in a parameter table; section 4.3: what a captured CUDA graph reads
+ * must live in device memory so that the graph stays valid as requests
+ * change).  Everything the launch depends on is in device memory: the
+ * records, the row counts and the tensor maps, which a first small kernel
+ * builds from the records on the device; a graph captured once therefore
+ * computes whatever groups the table and Ms hold at each replay.
+ *
+ * groups:    DEVICE array of G fp8_group_desc (8-byte aligned), read by the
+ *            launch's kernels; the pointers follow fp8_group_desc's layouts.
+ * Ms:        DEVICE int32[G] row counts (M_g < 0 counts as 0).
+ * N, K:      shared by all groups, multiples of 32; K = 0 gives FP8_ERR_SHAPE.
+ * workspace: DEVICE memory of at least fp8_grouped_workspace_bytes(G) bytes,
+ *            128-byte aligned, caller-owned, holding the per-group tensor
+ *            maps between the two kernels; launches that overlap on the GPU
+ *            need separate workspaces.
+ * A record with a null pointer, or A, B or C not 16-byte aligned, or sA or
+ * sB not 4-byte aligned, is rejected on the device: its group is skipped
+ * (its C is not written) and FP8_ERR_RECORD is recorded for
+ * fp8_status_query.  Results equal fp8_gemm_grouped's for the same records,
+ * bit for bit.  AUTO path.  G > FP8_MAX_GROUPS_PER_LAUNCH is split into
+ * consecutive launch pairs.  Returns FP8_OK or FP8_ERR_SHAPE / FP8_ERR_NULL /
+ * FP8_ERR_ALIGN (groups, Ms or workspace) / FP8_ERR_CUDA. */
+int fp8_gemm_grouped_device(const fp8_group_desc *groups, const int32_t *Ms, int64_t N, int64_t K,
+                            int32_t G, void *workspace, int64_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes fp8_gemm_grouped_device needs for G groups (0 for G < 0). */
+int64_t fp8_grouped_workspace_bytes(int32_t G);
+
 /* Synchronises `stream`, then reads and clears the current device's status
- * words: the one the regular entry points write and word 0 of the
+ * words: the one the regular entry points write (including FP8_ERR_RECORD
+ * from fp8_gemm_grouped_device) and word 0 of the
  * allocation-free entry point's static array (each only once its entry point
  * has run on this device).  Allocates nothing.  *status = FP8_OK, or the
  * FP8_ERR_* code of a condition recorded since the last query
- * (FP8_ERR_TIMEOUT takes precedence over FP8_ERR_SCALE).  The status comes
+ * (FP8_ERR_TIMEOUT takes precedence, then FP8_ERR_RECORD, then FP8_ERR_SCALE).  The status comes
  * back through the out-pointer so that the return value stays the call's own
  * FP8_OK / FP8_ERR_CUDA / FP8_ERR_NULL. */
 int fp8_status_query(cudaStream_t stream, int *status);

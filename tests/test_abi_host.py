@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_strerror(lib):
     assert bs.fp8_version() == 10000
-    for code in range(0, -9, -1):
+    for code in range(0, -10, -1):
         assert bs.fp8_strerror(code).startswith("FP8_")
     assert "unknown" in bs.fp8_strerror(-99)
 
@@ -129,3 +129,19 @@ def test_binding_raises_on_error(lib):
     with pytest.raises(bs.Fp8Error) as e:
         bs.fp8_gemm_blockscaled(T(16), T(16), T(16, (33, 64)), T(16), T(16), stream=0)
     assert e.value.code == _abi.FP8_ERR_SHAPE
+
+
+def test_grouped_device_argument_errors(lib):
+    """fp8_gemm_grouped_device checks its host-visible arguments before any
+    device work: sizes, null and misaligned pointers, a short workspace."""
+    need = lib.fp8_grouped_workspace_bytes(4)
+    assert need >= 4 * 128
+    assert lib.fp8_grouped_workspace_bytes(-1) == 0
+    f = lib.fp8_gemm_grouped_device
+    assert f(256, 256, 64, 64, -1, 256, need, None) == _abi.FP8_ERR_SHAPE
+    assert f(256, 256, 48, 64, 4, 256, need, None) == _abi.FP8_ERR_SHAPE
+    assert f(0, 0, 64, 64, 0, 0, 0, None) == _abi.FP8_OK            # G = 0: nothing to do
+    assert f(256, 256, 0, 64, 4, 256, need, None) == _abi.FP8_OK    # N = 0: nothing to do
+    assert f(256, 256, 64, 64, 4, 0, need, None) == _abi.FP8_ERR_NULL
+    assert f(256, 256, 64, 64, 4, 256 + 64, need, None) == _abi.FP8_ERR_ALIGN
+    assert f(256, 256, 64, 64, 4, 256, need - 1, None) == _abi.FP8_ERR_SHAPE
