@@ -112,3 +112,32 @@ def test_quantize_rounding_midpoints(bs):
     q_ref, s_ref = oracle.quantize_blocks(_bits(both.contiguous()), M, K)
     assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
     assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
+def test_quantize_wide_exponents_and_subnormal_scales(bs):
+    """Every block gets its own maximum, from 2^-133 (a bf16 subnormal, whose
+    scale amax/448 is an fp32 subnormal) up to 2^120, and random bf16 values
+    below it, zeros and negative zeros included: the codes and scales match
+    the oracle's fp32 division bit for bit on both sides of the normal-scale
+    boundary."""
+    rng = np.random.default_rng(33)
+    MB, KB = 8, 64                                   # 512 blocks of 32 x 32
+    exps = np.linspace(-133, 120, MB * KB).round().astype(int)
+    rng.shuffle(exps)
+    x = np.empty((MB * 32, KB * 32), dtype=np.float32)
+    for b, e in enumerate(exps):
+        mb, kb = divmod(b, KB)
+        amax = np.float32(2.0 ** e) * np.float32(rng.uniform(1.0, 2.0))
+        blk = rng.uniform(-1.0, 1.0, size=(32, 32)).astype(np.float32) * amax
+        blk[0, 0] = amax
+        blk[1, 1] = 0.0
+        blk[2, 2] = -0.0
+        x[mb * 32:(mb + 1) * 32, kb * 32:(kb + 1) * 32] = blk
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    M, K = xb.shape
+    q, s = bs.fp8_quantize_blocks(xb.to(DEV))
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quantize_blocks(_bits(xb.contiguous()), M, K)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert (s_ref < np.float32(1.17549435e-38)).any() and (s_ref > 1.0).any()
