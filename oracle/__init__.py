@@ -71,6 +71,8 @@ def _load():
         lib.oracle_gemm_rowcol.restype = ctypes.c_int
         lib.oracle_quantize_blocks.argtypes = [dp, i64, i64, u8p, fp]
         lib.oracle_quantize_blocks.restype = ctypes.c_int
+        lib.oracle_gemm_pertoken.argtypes = [u8p, fp, u8p, fp, i64, i64, i64, dp, dp, ctypes.c_int]
+        lib.oracle_gemm_pertoken.restype = ctypes.c_int
         lib.oracle_gemm_residual.argtypes = [u8p, fp, u8p, fp, dp, i64, i64, i64, dp, dp,
                                              ctypes.c_int, ctypes.c_int]
         lib.oracle_gemm_residual.restype = ctypes.c_int
@@ -258,4 +260,23 @@ def gemm_residual_sampled(A, sA, B, sB, R_bits, M: int, N: int, K: int, ms, ns, 
                                               _ptr(ms), _ptr(ns), ms.size, _ptr(C), _ptr(T), int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_residual_sampled failed ({rc})")
+    return C, T
+
+
+def gemm_pertoken(A, sA, B, sB, M: int, N: int, K: int, mutation: int = 0):
+    """Per-token A scales: C[m,n] = sum_kb sA[m,kb]*sB[n//32,kb]*sum_{k in kb}
+    A[m,k]*B[n,k] with sA [M, K/32] and sB [ceil(N/32), K/32] fp32.  Returns
+    (C, T) in fp64 like gemm().  ``mutation`` != 0: pin tests only."""
+    KB = K // 32
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    A = _codes(A, M, K)
+    B = _codes(B, N, K)
+    sA = np.ascontiguousarray(np.asarray(sA, dtype=np.float32).reshape(M, KB))
+    sB = _scales(sB, N, KB)
+    C = np.zeros((M, N), dtype=np.float64)
+    T = np.zeros((M, N), dtype=np.float64)
+    if _load().oracle_gemm_pertoken(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), M, N, K,
+                                    _ptr(C), _ptr(T), int(mutation)) != 0:
+        raise ValueError("oracle_gemm_pertoken: bad arguments")
     return C, T

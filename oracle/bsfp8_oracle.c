@@ -366,3 +366,45 @@ int oracle_gemm_residual_sampled(const uint8_t *A, const float *sA, const uint8_
     for (int64_t i = 0; i < count; ++i) C[i] += residual_term(R, N, ms[i], ns[i], 0);
     return 0;
 }
+
+/* ------------------------------------------------ per-token A scales ---- */
+
+/* Per-token scales for A (FP8 GEMM library article, hncyxsy.com/news/241433,
+ * section 2.2: per-token scales for activations, the finer alternative to
+ * 32x32 blocks; here one scale per row of A per 32-K block, B keeping its
+ * 32x32 blocks):
+ *
+ *   C[m,n] = sum_kb sA[m][kb] * sB[n/32][kb] * sum_{k in kb} A[m,k] * B[n,k]
+ *
+ * sA is [M, K/32] row-major, sB [ceil(N/32), K/32].  The same arithmetic as
+ * oracle_gemm (exact 32-term sums in fp64, the exact product of the two fp32
+ * scales, fp64 accumulation in ascending kb); only the A scale's row index
+ * differs.  `mutation` 6 (pin tests only) reads the A scale of row
+ * 32*(m/32) instead of m. */
+int oracle_gemm_pertoken(const uint8_t *A, const float *sA, const uint8_t *B, const float *sB,
+                         int64_t M, int64_t N, int64_t K, double *C, double *T, int mutation) {
+    if (M < 0 || N < 0 || K < 0 || (K % 32) != 0) return -1;
+    double tab[256];
+    oracle_e4m3_table(tab);
+    const int64_t KB = K / 32;
+    for (int64_t m = 0; m < M; ++m) {
+        const int64_t ra = mutation == 6 ? 32 * (m / 32) : m;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t kb = 0; kb < KB; ++kb) {
+                double s = 0.0, sabs = 0.0;
+                for (int64_t k = kb * 32; k < kb * 32 + 32; ++k) {
+                    const double p = tab[A[m * K + k]] * tab[B[n * K + k]];
+                    s += p;
+                    sabs += fabs(p);
+                }
+                const double sc = (double)sA[ra * KB + kb] * (double)sB[(n / 32) * KB + kb];
+                acc += sc * s;
+                mag += fabs(sc) * sabs;
+            }
+            C[m * N + n] = acc;
+            T[m * N + n] = mag;
+        }
+    }
+    return 0;
+}

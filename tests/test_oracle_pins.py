@@ -551,3 +551,51 @@ def test_residual_sampled_equals_full():
     ns = rng.integers(0, N, 300)
     Cs, Ts = oracle.gemm_residual_sampled(A, sA, B, sB, R, M, N, K, ms, ns)
     assert np.array_equal(Cs, C[ms, ns]) and np.array_equal(Ts, T[ms, ns])
+
+
+# ----------------------------------------------------- per-token A scales ----
+
+def test_pertoken_with_block_constant_scales_equals_block_oracle():
+    """Per-row scales equal within each 32-row block are the 32x32 block
+    case: the two oracles agree exactly."""
+    M, N, K = 70, 64, 160
+    A, sA, B, sB = _rand_problem(M, N, K, seed=31, arbitrary=True)
+    sA_tok = np.repeat(sA, 32, axis=0)[:M]
+    C1, T1 = oracle.gemm(A, sA, B, sB, M, N, K)
+    C2, T2 = oracle.gemm_pertoken(A, sA_tok, B, sB, M, N, K)
+    assert np.array_equal(C1, C2) and np.array_equal(T1, T2)
+
+
+def test_pertoken_brute_force_exact():
+    """Distinct power-of-two scales per row: every partial sum is exact, and
+    the oracle equals exact rational arithmetic; a per-row scale read from
+    the wrong row (mutation 6) fails it."""
+    M, N, K = 37, 33, 96
+    rng = np.random.default_rng(32)
+    A, _, B, sB = _rand_problem(M, N, K, seed=32, elo=-2, ehi=2)
+    sA = np.ldexp(1.0, rng.integers(-2, 3, (M, K // 32))).astype(np.float32)
+    tab = oracle.e4m3_table()
+    C, _ = oracle.gemm_pertoken(A, sA, B, sB, M, N, K)
+    Cm, _ = oracle.gemm_pertoken(A, sA, B, sB, M, N, K, mutation=6)
+    mismatches = 0
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(float(sA[m, k // 32])) * Fraction(float(sB[n // 32, k // 32]))
+                        * Fraction(tab[A[m, k]]) * Fraction(tab[B[n, k]]) for k in range(K))
+            assert Fraction(C[m, n]) == exact
+            mismatches += Fraction(Cm[m, n]) != exact
+    assert mismatches > 0
+
+
+def test_pertoken_row_scaling_closed_form():
+    """Scales constant along K for each row (per token) and unit B scales:
+    C = diag(sA) (A B^T), the fp64 matmul of the decoded codes (exact)."""
+    M, N, K = 45, 64, 128
+    A, _, B, _ = _rand_problem(M, N, K, seed=33)
+    rng = np.random.default_rng(33)
+    a = np.ldexp(1.0, rng.integers(-5, 6, M))
+    sA = np.repeat(a[:, None], K // 32, axis=1).astype(np.float32)
+    sB = np.ones((N // 32, K // 32), np.float32)
+    tab = oracle.e4m3_table()
+    C, _ = oracle.gemm_pertoken(A, sA, B, sB, M, N, K)
+    assert np.array_equal(C, a[:, None] * (tab[A] @ tab[B].T))
