@@ -16,7 +16,7 @@ from ._abi import (FP8_PATH_AUTO, FP8_PATH_NATIVE, FP8_PATH_PROMOTE,  # noqa: F4
                    FP8_MAX_GROUPS_PER_LAUNCH, fp8_group_desc)
 
 __all__ = ["fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_gemm_grouped", "group_descs",
-           "fp8_gemm_grouped_device", "fp8_grouped_workspace_bytes", "group_table",
+           "fp8_gemm_grouped_device", "fp8_grouped_workspace_bytes", "group_table", "fp8_gemm_pertoken",
            "fp8_quantize_blocks", "fp8_gemm_rowcol", "fp8_gemm_blockscaled_residual",
            "fp8_status_query", "fp8_strerror", "fp8_version", "fp8_debug_set", "fp8_lib_shutdown",
            "Fp8Error", "library"]
@@ -102,6 +102,17 @@ def fp8_gemm_rowcol(A, sA, B, sB, C, M=None, N=None, K=None, stream=None):
     N = B.shape[0] if N is None else N
     _check(library().fp8_gemm_rowcol(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C), M, N, K,
                                      _stream(stream)), "fp8_gemm_rowcol")
+    return C
+
+
+def fp8_gemm_pertoken(A, sA, B, sB, C, M=None, N=None, K=None, stream=None):
+    """C[M,N] (bf16) with per-token A scales: sA fp32 [M, K/32] (one per row
+    of A per 32-K block), sB fp32 [N/32, K/32] blocks."""
+    M = A.shape[0] if M is None else M
+    K = A.shape[1] if K is None else K
+    N = B.shape[0] if N is None else N
+    _check(library().fp8_gemm_pertoken(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C), M, N, K,
+                                       _stream(stream)), "fp8_gemm_pertoken")
     return C
 
 

@@ -56,6 +56,9 @@ int set_kernel_attrs() {
     if (cudaFuncSetAttribute(bsfp8_gemm_plain<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN>()) != cudaSuccess)
         return FP8_ERR_CUDA;
+    if (cudaFuncSetAttribute(bsfp8_gemm_plain<BN, SCALE_TOKEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<BN>()) != cudaSuccess)
+        return FP8_ERR_CUDA;
     if (cudaFuncSetAttribute(bsfp8_gemm_grouped<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN, false, true>()) != cudaSuccess)
         return FP8_ERR_CUDA;
@@ -273,7 +276,7 @@ void fill_common(Common &c, int64_t M, int64_t N, int64_t K, int mode, DeviceSta
     }
 }
 
-template <int BN>
+template <int BN, int SK = SCALE_BLOCK32>
 int launch_plain(const void *A, const float *sA, const void *B, const float *sB, void *C,
                  int64_t M, int64_t N, int64_t K, int mode, DeviceState *d, cudaStream_t stream) {
     PlainArgs args;
@@ -290,7 +293,7 @@ int launch_plain(const void *A, const float *sA, const void *B, const float *sB,
     args.e.sB = sB;
     args.e.C = static_cast<__nv_bfloat16 *>(C);
     int grid = args.c.num_tiles < d->sm_count ? args.c.num_tiles : d->sm_count;
-    bsfp8_gemm_plain<BN><<<grid, NUM_THREADS, smem_bytes<BN>(), stream>>>(args);
+    bsfp8_gemm_plain<BN, SK><<<grid, NUM_THREADS, smem_bytes<BN>(), stream>>>(args);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -583,6 +586,27 @@ int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *
     if (rc != FP8_OK) return rc;
     if (K == 0) return zero_fill(C, M * N, stream);
     return launch_pair<TILE_N, SCALE_ROWCOL, false>(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, d, stream);
+}
+
+int fp8_gemm_pertoken(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                      int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != FP8_OK) return rc;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!C) return FP8_ERR_NULL;
+    if (!aligned(C, 16)) return FP8_ERR_ALIGN;
+    if (K > 0) {
+        if (!A || !B || !sA || !sB) return FP8_ERR_NULL;
+        if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 4) || !aligned(sB, 4))
+            return FP8_ERR_ALIGN;
+    }
+    DeviceState *d = nullptr;
+    rc = device_setup(&d);
+    if (rc != FP8_OK) return rc;
+    if (K == 0) return zero_fill(C, M * N, stream);
+    // per-row scales take the promotion path on single-CTA tiles (faster for
+    // that path than CTA pairs)
+    return launch_plain<TILE_N, SCALE_TOKEN>(A, sA, B, sB, C, M, N, K, FP8_PATH_PROMOTE, d, stream);
 }
 
 int fp8_gemm_blockscaled_noalloc(const void *A, const float *sA, const void *B, const float *sB,

@@ -95,7 +95,10 @@ enum : int { PATH_AUTO = 0, PATH_NATIVE = 1, PATH_PROMOTE = 2 };
 // SCALE_BLOCK32: sA [ceil(M/32)][K/32], sB [N/32][K/32] block scales.
 // SCALE_ROWCOL: sA [M] and sB [N], constant along K: the MMAs run with unit
 // scales and the epilogue multiplies each output by sA[m] * sB[n].
-enum : int { SCALE_BLOCK32 = 0, SCALE_ROWCOL = 1 };
+// SCALE_TOKEN: sA [M][K/32], one scale per row of A per 32-K block (per token),
+// sB [N/32][K/32] blocks: always the promotion path, the epilogue thread of
+// row m reading sA[m][kb] itself.
+enum : int { SCALE_BLOCK32 = 0, SCALE_ROWCOL = 1, SCALE_TOKEN = 2 };
 
 template <int BN_, bool PAIR_ = false, bool GROUPED_ = false>
 struct Cfg {
@@ -971,6 +974,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             int verdict = 1;
             if constexpr (SK == SCALE_ROWCOL) {
                 verdict = 0;   // unit block scales: the native path
+            } else if constexpr (SK == SCALE_TOKEN) {
+                verdict = 1;   // per-row scales: the promotion path
             } else if (c.mode != PATH_PROMOTE) {
                 bool any_bad;
                 if (i == 0) {
@@ -1097,7 +1102,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     const GroupEntry e = sch.entry(tt.g);
                     const int mb = (tt.m0 + row_off) / 32 + (lane >> 2);
                     const int nb = tt.n0 / 32 + (lane >> 2);
-                    a_in = lane < 16 && mb < (tt.Mg + 31) / 32;
+                    a_in = lane < 16 && mb < (tt.Mg + 31) / 32 && SK != SCALE_TOKEN;   // (per-row sA: read by the epilogue)
                     b_in = lane < 4 * NBB && nb < c.N / 32;
                     pa = e.sA + (a_in ? static_cast<int64_t>(mb) * c.KB + (lane & 3) : 0);
                     pb = e.sB + (b_in ? static_cast<int64_t>(nb) * c.KB + (lane & 3) : 0);
@@ -1266,7 +1271,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     // scale products sA * sB of this K block, one per 32-column block
                     const float *se = sm_sc + f * C::SC_ENTRY + hh * C::SC_FLOATS;
                     static_assert(NCH == 4, "one 16-byte load of column scales per K block");
-                    const float sa = se[j * 4 + q];
+                    float sa;
+                    if constexpr (SK == SCALE_TOKEN) sa = row_ok ? __ldg(e.sA + static_cast<int64_t>(row) * c.KB + kb) : 0.0f;
+                    else sa = se[j * 4 + q];
                     const float4 sb = *reinterpret_cast<const float4 *>(se + 16 + j * NBB + h * NCH);
                     const float sc[NCH] = {sa * sb.x, sa * sb.y, sa * sb.z, sa * sb.w};
                     if (++j == KB_PER_STAGE) {
@@ -1363,10 +1370,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     }
 }
 
-template <int BN>
+template <int BN, int SK = SCALE_BLOCK32>
 __global__ void __launch_bounds__(NUM_THREADS, 1) bsfp8_gemm_plain(const __grid_constant__ PlainArgs args) {
     extern __shared__ uint8_t smem_raw[];
-    gemm_body<BN, false, false>(args, smem_raw);
+    gemm_body<BN, false, false, PlainArgs, SK>(args, smem_raw);
 }
 
 // CTA-pair variant: clusters of two CTAs, 256-row tiles, pair MMAs.

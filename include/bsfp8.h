@@ -131,6 +131,22 @@ int fp8_gemm_blockscaled_residual(const void *A, const float *sA, const void *B,
 int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *sB, void *C,
                     int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
+/* Block-scaled GEMM with per-token scales for A (FP8 GEMM library article,
+ * hncyxsy.com/news/241433, section 2.2: per-token scales for activations, a
+ * finer granularity than 32x32 blocks): one fp32 scale per row of A per
+ * 32-K block, B keeping its 32x32 blocks:
+ *   C[m,n] = bf16( sum_kb sA[m][kb] * sB[n/32][kb] * sum_{k in kb} A[m,k]*B[n,k] )
+ * sA: fp32 [M, K/32] row-major (4-byte aligned); everything else as
+ * fp8_gemm_blockscaled.  Any finite scales: every tile takes the per-K-block
+ * fp32 promotion (unscaled 32-deep tensor-core partials, acc += (sA*sB) *
+ * partial in fp32, K ascending), so each row's bits are the same for every M.
+ * With scales equal within each 32-row block the result equals
+ * fp8_gemm_blockscaled_ex(..., FP8_PATH_PROMOTE) on the block scales, bit for
+ * bit.  Returns FP8_OK or FP8_ERR_SHAPE / FP8_ERR_NULL / FP8_ERR_ALIGN /
+ * FP8_ERR_CUDA. */
+int fp8_gemm_pertoken(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                      int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* Block quantization of activations to the operand format above (FP8 GEMM
  * library article, hncyxsy.com/news/241433, section 2.1: E4M3, largest value
  * 448; section 2.2: one scale per 32x32 block).  For each 32x32 block of x:

@@ -1,0 +1,105 @@
+"""GPU parity of the GEMM with per-token A scales (fp8_gemm_pertoken, through
+the C ABI): one fp32 scale per row of A per 32-K block, B with 32x32 blocks
+(FP8 GEMM library article, hncyxsy.com/news/241433, section 2.2), against
+the oracle's oracle_gemm_pertoken element by element; the block-constant
+case against the block-scaled call bit for bit; rows bit-identical across M."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._accept import bf16_to_f64, check
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def bs():
+    import block_scaled_fp8_sm_gb300 as mod
+    from block_scaled_fp8_sm_gb300 import build
+    build.build()
+    mod.library()
+    return mod
+
+
+def _problem(M, N, K, seed, pow2=False):
+    g = torch.Generator().manual_seed(seed)
+    A = workloads.normal_codes(M, K, g, "cpu")
+    B = workloads.normal_codes(N, K, g, "cpu")
+    if pow2:
+        sA = torch.ldexp(torch.ones(M, K // 32), torch.randint(-4, 5, (M, K // 32), generator=g)).float()
+        sB = workloads.pow2_scales(N, K // 32, -4, 4, g, "cpu")
+    else:
+        sA = torch.rand(M, K // 32, generator=g) * 2 + 0.05
+        sB = torch.rand(N // 32, K // 32, generator=g) * 2 + 0.05
+    return A, sA.contiguous(), B, sB.contiguous()
+
+
+def _run(bs, A, sA, B, sB, M, N, K):
+    buf = torch.full((M + 2, N), -7.0, dtype=torch.bfloat16, device=DEV)
+    C = buf[1:M + 1]
+    bs.fp8_gemm_pertoken(A.to(DEV), sA.to(DEV), B.to(DEV), sB.to(DEV), C, M, N, K)
+    torch.cuda.synchronize()
+    assert torch.all(buf[0] == -7.0) and torch.all(buf[-1] == -7.0), "store outside C"
+    return C
+
+
+@pytest.mark.parametrize("M,N,K,pow2", [(1, 32, 32, False), (45, 96, 160, False), (130, 288, 480, True),
+                                        (300, 512, 1056, False), (257, 256, 2048, True)])
+def test_pertoken_parity(bs, M, N, K, pow2):
+    A, sA, B, sB = _problem(M, N, K, seed=M + N + K, pow2=pow2)
+    C = _run(bs, A, sA, B, sB, M, N, K)
+    Cr, T = oracle.gemm_pertoken(A.numpy(), sA.numpy(), B.numpy(), sB.numpy(), M, N, K)
+    check(bf16_to_f64(C), Cr, T, f"pertoken {M}x{N}x{K}{' pow2' if pow2 else ''}")
+    assert bs.fp8_status_query() == 0
+
+
+def test_block_constant_scales_equal_the_block_scaled_promotion(bs):
+    M, N, K = 1000, 512, 1024
+    A, _, B, sB = _problem(M, N, K, seed=5)
+    g = torch.Generator().manual_seed(6)
+    sA_blk = torch.rand((M + 31) // 32, K // 32, generator=g) + 0.1
+    sA_tok = sA_blk.repeat_interleave(32, dim=0)[:M].contiguous()
+    C_tok = _run(bs, A, sA_tok, B, sB, M, N, K)
+    C_blk = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    bs.fp8_gemm_blockscaled(A.to(DEV), sA_blk.to(DEV), B.to(DEV), sB.to(DEV), C_blk, M, N, K, mode=bs.FP8_PATH_PROMOTE)
+    torch.cuda.synchronize()
+    assert torch.equal(C_tok.view(torch.int16), C_blk.view(torch.int16))
+
+
+def test_pertoken_batch_invariance(bs):
+    M, N, K = 4096, 512, 1024
+    A, sA, B, sB = _problem(M, N, K, seed=7)
+    dB, dsB = B.to(DEV), sB.to(DEV)
+    rows = {}
+    for m in (1, 7, 64, M):
+        C = torch.empty(m, N, dtype=torch.bfloat16, device=DEV)
+        bs.fp8_gemm_pertoken(A[:m].contiguous().to(DEV), sA[:m].contiguous().to(DEV), dB, dsB, C, m, N, K)
+        torch.cuda.synchronize()
+        rows[m] = C[:64].view(torch.int16).cpu()
+    for m in (1, 7, 64):
+        k = min(m, 64)
+        assert torch.equal(rows[m][:k], rows[M][:k]), f"M={m}"
+    Cr, T = oracle.gemm_pertoken(A[:64].numpy(), sA[:64].numpy(), B.numpy(), sB.numpy(), 64, N, K)
+    check(bf16_to_f64(rows[M].view(torch.bfloat16)), Cr, T, "pertoken batch invariance rows")
+
+
+def test_pertoken_square_4096_sampled(bs):
+    M = N = K = 4096
+    g = torch.Generator(device=DEV).manual_seed(8)
+    A = workloads.normal_codes(M, K, g, DEV)
+    B = workloads.normal_codes(N, K, g, DEV)
+    sA = torch.rand(M, K // 32, generator=g, device=DEV) + 0.05
+    sB = torch.rand(N // 32, K // 32, generator=g, device=DEV) + 0.05
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    bs.fp8_gemm_pertoken(A, sA, B, sB, C, M, N, K)
+    torch.cuda.synchronize()
+    assert bs.fp8_status_query() == 0
+    rng = np.random.default_rng(8)
+    rows = np.unique(np.concatenate([[0, 127, 128, 2049, M - 1], rng.integers(0, M, 60)]))
+    Ah, sAh, Bh, sBh = (t.cpu().numpy() for t in (A, sA, B, sB))
+    Cr, T = oracle.gemm_pertoken(Ah[rows], sAh[rows], Bh, sBh, len(rows), N, K)   # whole rows
+    Cg = C[torch.from_numpy(rows).to(DEV)]
+    check(bf16_to_f64(Cg), Cr, T, "pertoken 4096^3 rows")
