@@ -10,7 +10,9 @@
 // 512 contiguous bytes and every warp-row store 256.  Block b of the strip is
 // held by lanes 4b..4b+3 of all eight warps: its maximum is reduced over those
 // four lanes with shuffles, then over the warps through shared memory.
-// Both divisions are correctly rounded fp32 divisions.
+// s is a correctly rounded fp32 division.  The element quotients x/s share one
+// reciprocal per block (quotient() below), which takes a third of the issue
+// slots of a division per element.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -19,6 +21,23 @@ namespace bsfp8 {
 
 constexpr int QT_COLS = 256;
 constexpr int QT_THREADS = 256;
+
+// x/s from r = RN(1/s): y = RN(x r), then Markstein's correction
+// q = RN(y + r RN(x - y s)) (P. Markstein, IBM J. Res. Develop. 34(1), 1990,
+// the division theorem), which is RN(x/s) whenever the residual x - y s is
+// exact.  Used for finite scales s >= 2^-100 only.  Enumerating every positive
+// bf16 block maximum (s = RN(amax/448)) and every bf16 x with |x| <= amax
+// gives: q == RN(x/s) bit for bit wherever |x/s| >= 2^-10, and below 2^-10
+// (subnormal x, underflowing quotients) both lie under half the smallest E4M3
+// subnormal, so the code is +-0 either way -- the codes equal those of the
+// correctly rounded division for every input.  Below 2^-100, x may be subnormal
+// next to quotients that matter, and the kernel divides.
+__device__ __forceinline__ float quotient(float x, float s, float r) {
+    const float y = __fmul_rn(x, r);
+    const float e = __fmaf_rn(-y, s, x);
+    const float q = __fmaf_rn(e, r, y);
+    return x == 0.0f ? x : q;   // keeps the sign of a zero
+}
 
 // Two fp32 values -> two E4M3 codes (nearest-even, saturating), lo in byte 0.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -62,15 +81,27 @@ __global__ void __launch_bounds__(QT_THREADS) bsfp8_quantize_blocks(const __nv_b
         __syncthreads();   // part is rewritten by the next row block
         const float sc = bmax > 0.0f ? __fdiv_rn(bmax, 448.0f) : 1.0f;
         if (warp == 0 && (lane & 3) == 0 && col_ok) s[mb * KB + col / 32] = sc;
+        // The branch is uniform over the lanes of a block, and taken once per
+        // 32 elements rather than per element.
+        if (sc >= 0x1p-100f && sc <= 3.40282347e38f) {
+            const float rc = __frcp_rn(sc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[i][j] = quotient(v[i][j], sc, rc);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[i][j] = __fdiv_rn(v[i][j], sc);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int64_t r = mb * 32 + warp + 8 * i;
             if (!(col_ok && r < M)) continue;
             uint2 out;
-            out.x = e4m3x2(__fdiv_rn(v[i][0], sc), __fdiv_rn(v[i][1], sc)) |
-                    (e4m3x2(__fdiv_rn(v[i][2], sc), __fdiv_rn(v[i][3], sc)) << 16);
-            out.y = e4m3x2(__fdiv_rn(v[i][4], sc), __fdiv_rn(v[i][5], sc)) |
-                    (e4m3x2(__fdiv_rn(v[i][6], sc), __fdiv_rn(v[i][7], sc)) << 16);
+            out.x = e4m3x2(v[i][0], v[i][1]) | (e4m3x2(v[i][2], v[i][3]) << 16);
+            out.y = e4m3x2(v[i][4], v[i][5]) | (e4m3x2(v[i][6], v[i][7]) << 16);
             *reinterpret_cast<uint2 *>(q + r * K + col) = out;
         }
     }
