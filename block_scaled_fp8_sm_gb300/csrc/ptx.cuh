@@ -311,6 +311,17 @@ __device__ __forceinline__ void f32x2_unpack(uint64_t v, uint32_t &lo, uint32_t 
 __device__ __forceinline__ void fma_f32x2(uint64_t &acc, uint64_t a, uint64_t b) {
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
+// a * b + c and a * b on both halves, rounded to nearest even
+__device__ __forceinline__ uint64_t fma_f32x2_rn(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2_rn(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 
 // ----------------------------------------------------------- descriptors ----
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle

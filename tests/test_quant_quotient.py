@@ -1,14 +1,17 @@
-"""CPU proof by enumeration that the block quantizer's reciprocal quotient codes
-every input as the correctly rounded division does.
+"""CPU proof by enumeration that the block quantizer's scale and reciprocal
+quotient code every input as the correctly rounded divisions do.
 
 The quantizer (FP8 GEMM library article, hncyxsy.com/news/241433, sections
-2.1-2.2: s = amax/448 per 32x32 block, q = E4M3(x/s)) forms x/s from one
-reciprocal per block plus Markstein's correction (P. Markstein, IBM J. Res.
-Develop. 34(1), 1990) for scales s >= 2^-100, and divides below that.  Both x
-and amax are bf16, so quotient_exhaustive.c enumerates every (amax, x) pair in
-IEEE fp32 with fused multiply-adds -- the same correctly rounded operations the
-kernel issues -- and compares quotient and E4M3 code with those of RN(x/s).
-The GPU quantizer tests then check the kernel itself against the oracle."""
+2.1-2.2: s = amax/448 per 32x32 block, q = E4M3(x/s)) forms s from the
+constant RN(1/448) and x/s from one reciprocal per block, each corrected by
+Markstein's method (P. Markstein, IBM J. Res. Develop. 34(1), 1990); the
+quotient is taken negated (packed f32x2 form) and the code's sign bit flipped.
+Scales below 2^-100 divide.  Both x and amax are bf16, so
+quotient_exhaustive.c enumerates every (amax, x) pair in IEEE fp32 with fused
+multiply-adds -- the same correctly rounded operations the kernel issues -- and
+compares scale, quotient and E4M3 code with those of the correctly rounded
+divisions.  The GPU quantizer tests then check the kernel itself against the
+oracle."""
 import os
 import shutil
 import subprocess
@@ -34,8 +37,8 @@ def _run(exe, t_log2, lo, hi):
     nt = max(1, min(32, os.cpu_count() or 1))
     out = subprocess.run([exe, str(t_log2), str(lo), str(hi), str(nt)], check=True, capture_output=True,
                          text=True, timeout=900).stdout.split()
-    pairs, bad_q, bad_big, bad_code = (int(v) for v in out)
-    return pairs, bad_q, bad_big, bad_code
+    pairs, bad_q, bad_big, bad_code, bad_scale = (int(v) for v in out)
+    return pairs, bad_q, bad_big, bad_code, bad_scale
 
 
 def _bf16_bits_of(v: float) -> int:
@@ -44,11 +47,12 @@ def _bf16_bits_of(v: float) -> int:
 
 
 def test_reciprocal_quotient_codes_every_input(prog):
-    """Threshold 2^-100: every quotient of size >= 2^-10 is the correctly
-    rounded one and every code agrees, over all 1.06e9 (amax, x) pairs whose
-    scale takes the reciprocal path."""
-    pairs, bad_q, bad_big, bad_code = _run(prog, -100, 1, AMAX_MAX)
+    """Threshold 2^-100: every scale equals RN(amax/448); every quotient of
+    size >= 2^-10 is the correctly rounded one and every code agrees, over all
+    1.06e9 (amax, x) pairs whose scale takes the reciprocal path."""
+    pairs, bad_q, bad_big, bad_code, bad_scale = _run(prog, -100, 1, AMAX_MAX)
     assert pairs > 1_000_000_000
+    assert bad_scale == 0
     assert bad_big == 0
     assert bad_code == 0
     # the remaining differences exist (subnormal x, underflowing quotients) and
@@ -61,7 +65,7 @@ def test_enumeration_catches_the_bare_normal_threshold(prog):
     reach codes that matter, and the enumeration must see code differences.
     Only the block maxima below 448 * 2^-100 are enumerated."""
     hi = _bf16_bits_of(448.0 * 2.0 ** -100)
-    pairs, bad_q, bad_big, bad_code = _run(prog, -126, 1, hi)
+    pairs, bad_q, bad_big, bad_code, _ = _run(prog, -126, 1, hi)
     assert pairs > 0
     assert bad_big > 0
     assert bad_code > 0
