@@ -57,6 +57,8 @@ WORKLOAD_NAMES = {
     "r1": "per-token x per-channel scaled E4M3 GEMM M=N=K=4096 (fp32 scales [M] and [N]), bf16 out",
     "f1": "block-scaled E4M3 GEMM M=N=K=4096 with a bf16 residual added in the epilogue",
     "p1": "per-token A scales (one fp32 per row per 32-K block) x 32x32 B blocks, E4M3 GEMM M=N=K=4096, bf16 out",
+    "p1n": "per-token power-of-two A scales (one per row per 32-K block, UE8M0 on the MMA) x 32x32 pow2 B blocks, "
+           "E4M3 GEMM M=N=K=4096 (mode NATIVE), bf16 out",
 }
 
 
@@ -226,16 +228,23 @@ def make_runner(name, dev, bs):
         def run(stream):
             bs.fp8_gemm_blockscaled_residual(p.A, p.sA, p.B, p.sB, R, C, p.M, p.N, p.K, stream=stream)
         return run, p.flops, p.algorithmic_bytes + 2 * p.M * p.N, {"A": p.A, "sA": p.sA, "B": p.B, "sB": p.sB, "R": R}
-    if name == "p1":
+    if name in ("p1", "p1n"):
         p = workloads.make("c1", seed=0, device=dev)
         g = torch.Generator(device=dev).manual_seed(2)
-        sA = torch.rand(p.M, p.K // 32, generator=g, device=dev) + 0.05
-        sB = torch.rand(p.N // 32, p.K // 32, generator=g, device=dev) + 0.05
+        if name == "p1":
+            sA = torch.rand(p.M, p.K // 32, generator=g, device=dev) + 0.05
+            sB = torch.rand(p.N // 32, p.K // 32, generator=g, device=dev) + 0.05
+            mode = None
+        else:
+            sA = torch.ldexp(torch.ones(p.M, p.K // 32, device=dev),
+                             torch.randint(-4, 5, (p.M, p.K // 32), generator=g, device=dev)).float()
+            sB = p.sB
+            mode = bs.FP8_PATH_NATIVE
         C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
         nbytes = p.M * p.K + p.N * p.K + 4 * (sA.numel() + sB.numel()) + 2 * p.M * p.N
 
         def run(stream):
-            bs.fp8_gemm_pertoken(p.A, sA, p.B, sB, C, p.M, p.N, p.K, stream=stream)
+            bs.fp8_gemm_pertoken(p.A, sA, p.B, sB, C, p.M, p.N, p.K, stream=stream, mode=mode)
         return run, p.flops, nbytes, {"A": p.A, "sA": sA, "B": p.B, "sB": sB}
     if name == "r1":
         p = workloads.make("c1", seed=0, device=dev)
@@ -592,7 +601,7 @@ def run_ours(args):
 
     results = {}
     hashes = {}
-    names = [HEADLINE] + ([] if args.headline_only else ["c1", "c3", "c4", "c4p", "q8", "r1", "f1", "p1"])
+    names = [HEADLINE] + ([] if args.headline_only else ["c1", "c3", "c4", "c4p", "q8", "r1", "f1", "p1", "p1n"])
     if args.only:
         names = [args.only]
     launches = 0
@@ -776,7 +785,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-elements", type=int, default=65536)
-    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "c4p", "q8", "r1", "f1", "p1"], default=None,
+    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "c4p", "q8", "r1", "f1", "p1", "p1n"], default=None,
                     help="time one workload only (no e2e, no CPU baseline): profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -105,14 +105,19 @@ def fp8_gemm_rowcol(A, sA, B, sB, C, M=None, N=None, K=None, stream=None):
     return C
 
 
-def fp8_gemm_pertoken(A, sA, B, sB, C, M=None, N=None, K=None, stream=None):
+def fp8_gemm_pertoken(A, sA, B, sB, C, M=None, N=None, K=None, stream=None, mode=None):
     """C[M,N] (bf16) with per-token A scales: sA fp32 [M, K/32] (one per row
-    of A per 32-K block), sB fp32 [N/32, K/32] blocks."""
+    of A per 32-K block), sB fp32 [N/32, K/32] blocks.  mode: None (AUTO) or
+    FP8_PATH_* (NATIVE: power-of-two scales on the block-scaled MMA)."""
     M = A.shape[0] if M is None else M
     K = A.shape[1] if K is None else K
     N = B.shape[0] if N is None else N
-    _check(library().fp8_gemm_pertoken(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C), M, N, K,
-                                       _stream(stream)), "fp8_gemm_pertoken")
+    if mode is None:
+        _check(library().fp8_gemm_pertoken(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C), M, N, K,
+                                           _stream(stream)), "fp8_gemm_pertoken")
+    else:
+        _check(library().fp8_gemm_pertoken_ex(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C), M, N, K,
+                                              mode, _stream(stream)), "fp8_gemm_pertoken_ex")
     return C
 
 

@@ -38,7 +38,7 @@ EXPORTS = (
     "fp8_gemm_grouped_ex", "fp8_status_query", "fp8_strerror", "fp8_version",
     "fp8_debug_set", "fp8_lib_shutdown", "fp8_gemm_blockscaled_noalloc",
     "fp8_quantize_blocks", "fp8_gemm_rowcol", "fp8_gemm_blockscaled_residual",
-    "fp8_gemm_grouped_device", "fp8_grouped_workspace_bytes", "fp8_gemm_pertoken",
+    "fp8_gemm_grouped_device", "fp8_grouped_workspace_bytes", "fp8_gemm_pertoken", "fp8_gemm_pertoken_ex",
 )
 
 
@@ -71,6 +71,8 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fp8_quantize_blocks.restype = ci
     lib.fp8_gemm_pertoken.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
     lib.fp8_gemm_pertoken.restype = ci
+    lib.fp8_gemm_pertoken_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
+    lib.fp8_gemm_pertoken_ex.restype = ci
     lib.fp8_gemm_rowcol.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
     lib.fp8_gemm_rowcol.restype = ci
     lib.fp8_gemm_blockscaled_residual.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp]

@@ -74,6 +74,10 @@ int set_kernel_attrs() {
     if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN, SCALE_BLOCK32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN, true>()) != cudaSuccess)
         return FP8_ERR_CUDA;
+    static_assert(smem_bytes<BN, true, false, true>() <= 232448, "shared memory of the per-token pair kernel");
+    if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN, SCALE_TOKEN, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<BN, true, false, true>()) != cudaSuccess)
+        return FP8_ERR_CUDA;
     return FP8_OK;
 }
 
@@ -328,7 +332,8 @@ int launch_pair(const void *A, const float *sA, const void *B, const float *sB, 
         if (rc != FP8_OK) return rc;
     }
     const int pairs = args.c.num_tiles < d->sm_count / 2 ? args.c.num_tiles : d->sm_count / 2;
-    bsfp8_gemm_pair<BN, SK, RES><<<2 * pairs, NUM_THREADS, smem_bytes<BN, true>(), stream>>>(args);
+    bsfp8_gemm_pair<BN, SK, RES><<<2 * pairs, NUM_THREADS, smem_bytes<BN, true, false, SK == SCALE_TOKEN>(), stream>>>(
+        args);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -588,9 +593,11 @@ int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *
     return launch_pair<TILE_N, SCALE_ROWCOL, false>(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, d, stream);
 }
 
-int fp8_gemm_pertoken(const void *A, const float *sA, const void *B, const float *sB, void *C,
-                      int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
-    int rc = check_shape(M, N, K);
+int fp8_gemm_pertoken_ex(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                         int64_t M, int64_t N, int64_t K, int mode, cudaStream_t stream) {
+    int rc = check_mode(mode);
+    if (rc != FP8_OK) return rc;
+    rc = check_shape(M, N, K);
     if (rc != FP8_OK) return rc;
     if (M == 0 || N == 0) return FP8_OK;
     if (!C) return FP8_ERR_NULL;
@@ -604,9 +611,17 @@ int fp8_gemm_pertoken(const void *A, const float *sA, const void *B, const float
     rc = device_setup(&d);
     if (rc != FP8_OK) return rc;
     if (K == 0) return zero_fill(C, M * N, stream);
-    // per-row scales take the promotion path on single-CTA tiles (faster for
-    // that path than CTA pairs)
+    // NATIVE: CTA pairs with per-row UE8M0 scale lines (the scales must be
+    // powers of two); otherwise the promotion path on single-CTA tiles (faster
+    // for that path than CTA pairs)
+    if (mode == FP8_PATH_NATIVE)
+        return launch_pair<TILE_N, SCALE_TOKEN, false>(A, sA, B, sB, C, M, N, K, FP8_PATH_NATIVE, d, stream);
     return launch_plain<TILE_N, SCALE_TOKEN>(A, sA, B, sB, C, M, N, K, FP8_PATH_PROMOTE, d, stream);
+}
+
+int fp8_gemm_pertoken(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                      int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    return fp8_gemm_pertoken_ex(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, stream);
 }
 
 int fp8_gemm_blockscaled_noalloc(const void *A, const float *sA, const void *B, const float *sB,

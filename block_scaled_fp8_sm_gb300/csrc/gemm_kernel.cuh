@@ -100,9 +100,12 @@ enum : int { PATH_AUTO = 0, PATH_NATIVE = 1, PATH_PROMOTE = 2 };
 // row m reading sA[m][kb] itself.
 enum : int { SCALE_BLOCK32 = 0, SCALE_ROWCOL = 1, SCALE_TOKEN = 2 };
 
-template <int BN_, bool PAIR_ = false, bool GROUPED_ = false>
+template <int BN_, bool PAIR_ = false, bool GROUPED_ = false, bool ROWA_ = false>
 struct Cfg {
     static constexpr int BN = BN_;
+    // Per-row A scale lines (per-token scales on the native path): 32 distinct
+    // 16-byte lines per 128-K half instead of 8 identical ones.
+    static constexpr bool ROWA = ROWA_;
     static constexpr bool PAIR = PAIR_;   // CTA pair (cta_group::2): 256-row tiles, B split by columns
     // Grouped (decode) tiles are 64 rows high: the A slots hold 64 rows, which
     // leaves room for a fifth operand stage (more weight bytes in flight).  The
@@ -126,7 +129,8 @@ struct Cfg {
     static constexpr int B_BYTES = HALVES * B_HALF;
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;           // 128 B rows per tcgen05.cp
     static constexpr int SF_SET = 128;                              // 8 lines x 16 B, read 4 times by tcgen05.cp
-    static constexpr int SF_BYTES = SF_SET * (1 + SFB_CHUNKS);      // scale lines per 128-K half
+    static constexpr int SF_SET_A = ROWA ? 512 : SF_SET;            // A's lines: 32 distinct or 8 identical
+    static constexpr int SF_BYTES = SF_SET_A + SF_SET * SFB_CHUNKS; // scale lines per 128-K half
     static constexpr int SF_COLS = 4 * (1 + SFB_CHUNKS);            // tensor-memory columns per stage
     static constexpr int SF_STAGES = PAIR ? 9 : 8;                  // scale ring entries (runs ahead of the
                                                                     // operand ring)
@@ -275,9 +279,9 @@ struct Tile {
     int m0, n0, Mg, g;
 };
 
-template <int BN, bool PAIR = false, bool GROUPED = false>
+template <int BN, bool PAIR = false, bool GROUPED = false, bool ROWA = false>
 constexpr int smem_bytes() {
-    using C = Cfg<BN, PAIR, GROUPED>;
+    using C = Cfg<BN, PAIR, GROUPED, ROWA>;
     return 1024 + C::STAGES * (C::A_BYTES + C::B_BYTES) + C::STG_BYTES +
            C::SF_STAGES * (C::SF_ENTRY + 4 * C::SC_ENTRY) +
            static_cast<int>(sizeof(Ctrl<C::STAGES, C::SF_STAGES>));
@@ -524,7 +528,9 @@ __device__ __forceinline__ void commit_to(uint64_t *bar) {
 // SK: scale layout; RES: a bf16 residual is added before the bf16 rounding.
 template <int BN, bool GROUPED, bool PAIR, typename Args, int SK = SCALE_BLOCK32, bool RES = false>
 __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
-    using C = Cfg<BN, PAIR, GROUPED>;
+    // per-token scales run the native path on CTA pairs (per-row scale lines)
+    // and the promotion path on single CTAs
+    using C = Cfg<BN, PAIR, GROUPED, PAIR && SK == SCALE_TOKEN>;
     static_assert(!(PAIR && GROUPED), "CTA pairs are used for single problems only");
     constexpr int S = C::STAGES;
     constexpr int NBB = C::NBB;
@@ -562,7 +568,9 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         }
         for (int f = 0; f < FS; ++f) {
             mbar_init(&ctl->scfull[f], 32);   // one cp.async arrival per scale-warp lane
-            mbar_init(&ctl->sfready[f], (PAIR && leader) ? 2 : 1);   // the leader also waits for the peer's lines
+            // the leader also waits for the peer's lines; per-row A lines are
+            // written by warp 2 besides the scale warp
+            mbar_init(&ctl->sfready[f], ((PAIR && leader) ? 2 : 1) + (C::ROWA ? 1 : 0));
             mbar_init(&ctl->sfempty[f], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -845,11 +853,13 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
 #pragma unroll
                         for (int hh = 0; hh < C::HALVES; ++hh) {
                             if (hh * KB_PER_STAGE < nk) {
-                                cp_lines<PAIR>(sfa + hh * C::SF_COLS, sdesc_sf_lines(sf_s + hh * C::SF_BYTES));
+                                cp_lines<PAIR>(sfa + hh * C::SF_COLS,
+                                               C::ROWA ? sdesc_sf_lines32(sf_s + hh * C::SF_BYTES)
+                                                       : sdesc_sf_lines(sf_s + hh * C::SF_BYTES));
 #pragma unroll
                                 for (int q = 0; q < C::SFB_CHUNKS; ++q)
                                     cp_lines<PAIR>(sfa + hh * C::SF_COLS + 4 + 4 * q,
-                                                   sdesc_sf_lines(sf_s + hh * C::SF_BYTES + C::SF_SET * (1 + q)));
+                                                   sdesc_sf_lines(sf_s + hh * C::SF_BYTES + C::SF_SET_A + C::SF_SET * q));
                             }
                         }
 #pragma unroll
@@ -965,34 +975,117 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         }
         __syncwarp();
     } else if (warp == 2) {
-        // -------------------------------------------------------- path verdict
-        for (int i = 0; i < my_tiles; ++i) {
-            const int v = i & 1;
-            bool ok = wait_bar(&ctl->vempty[v], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, ctl, c);
-            ok = __all_sync(FULL, ok);
-            if (!ok) break;
-            int verdict = 1;
-            if constexpr (SK == SCALE_ROWCOL) {
-                verdict = 0;   // unit block scales: the native path
-            } else if constexpr (SK == SCALE_TOKEN) {
-                verdict = 1;   // per-row scales: the promotion path
-            } else if (c.mode != PATH_PROMOTE) {
-                bool any_bad;
-                if (i == 0) {
-                    any_bad = ctl->first_bad != 0;   // computed by warps 1..11 at the start
-                } else {
-                    const Tile tt = sch.tile(unit + i * nunits);
-                    any_bad = __any_sync(FULL, tile_has_bad_scale<BN, C::TILE_M>(tt, sch.entry(tt.g), c, lane, 32));
+        if constexpr (C::ROWA) {
+            // ----------------------------------------------- per-row A scale lines
+            // Per-token A scales (one per row per 32-K block) on the native path.
+            // For each scale-ring entry lane l writes line l of each 128-K half:
+            // word w holds the UE8M0 scales of row 32w + l of this CTA's 128 rows,
+            // byte j that of K block j of the half, so tcgen05.cp hands every row
+            // its own scales.  The scales of entry e + 1 are loaded (plain loads
+            // into registers) before entry e's lines are written; a scale that is
+            // not a positive normal power of two sets the status word's scale bit.
+            // Every tile's verdict is the native path; it is published when the
+            // lines reach the tile (the verdict of tile i waits only for tile i - 2).
+            constexpr int H = C::HALVES;
+            const int KW = (c.KS + H - 1) / H;
+            const int total = my_tiles * KW;
+            auto load = [&](float (&dst)[H][16], int e) {
+                const int i = e / KW, ks = e - i * KW;
+                const Tile tt = sch.tile(unit + i * nunits);
+                const float *sa = sch.entry(tt.g).sA;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int row = tt.m0 + row_off + 32 * w + lane;
+                    const bool rin = row < tt.Mg;
+                    const float *pr = sa + static_cast<int64_t>(rin ? row : 0) * c.KB;
+#pragma unroll
+                    for (int h = 0; h < H; ++h)
+#pragma unroll
+                        for (int j = 0; j < KB_PER_STAGE; ++j) {
+                            const int kb = (ks * H + h) * KB_PER_STAGE + j;
+                            dst[h][4 * w + j] = (rin && kb < c.KB) ? __ldg(pr + kb) : 1.0f;
+                        }
                 }
-                verdict = any_bad ? 1 : 0;
-                if (any_bad && c.mode == PATH_NATIVE && lane == 0) atomicOr(c.status, STATUS_SCALE);
+            };
+            auto build = [&](const float (&src)[H][16], int e) -> bool {
+                const int i = e / KW, ks = e - i * KW;
+                if (ks == 0) {
+                    const int v = i & 1;
+                    if (!__all_sync(FULL, wait_bar(&ctl->vempty[v], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, ctl, c)))
+                        return false;
+                    if (lane == 0) {
+                        ctl->verdict[v] = 0;
+                        mbar_arrive(&ctl->vfull[v]);
+                        trace_event(c, TR_VERDICT, i);
+                    }
+                    __syncwarp();
+                }
+                const int f = e % FS;
+                if (!__all_sync(FULL, wait_bar(&ctl->sfempty[f], (static_cast<uint32_t>(e / FS) & 1u) ^ 1u, ctl, c)))
+                    return false;
+                bool bad = false;
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    uint32_t wd[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t x = 0;
+#pragma unroll
+                        for (int j = 0; j < KB_PER_STAGE; ++j) {
+                            const float v = src[h][4 * w + j];
+                            bad |= !is_pow2_scale(v);
+                            x |= ue8m0_of(v) << (8 * j);
+                        }
+                        wd[w] = x;
+                    }
+                    *reinterpret_cast<uint4 *>(sm_sf + f * C::SF_ENTRY + h * C::SF_BYTES + lane * 16) =
+                        make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                }
+                if (__any_sync(FULL, bad) && lane == 0) atomicOr(c.status, STATUS_SCALE);
+                fence_proxy_async_smem();   // the lines become visible to tcgen05.cp
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->sfready[f]);
+                __syncwarp();
+                return true;
+            };
+            float ra[H][16], rb[H][16];
+            if (total > 0) load(ra, 0);
+            for (int e = 0; e < total; e += 2) {
+                if (e + 1 < total) load(rb, e + 1);
+                if (!build(ra, e) || e + 1 >= total) break;
+                if (e + 2 < total) load(ra, e + 2);
+                if (!build(rb, e + 1)) break;
             }
-            if (lane == 0) {
-                ctl->verdict[v] = verdict;
-                mbar_arrive(&ctl->vfull[v]);
-                trace_event(c, TR_VERDICT, i);
+        } else {
+            // -------------------------------------------------------- path verdict
+            for (int i = 0; i < my_tiles; ++i) {
+                const int v = i & 1;
+                bool ok = wait_bar(&ctl->vempty[v], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, ctl, c);
+                ok = __all_sync(FULL, ok);
+                if (!ok) break;
+                int verdict = 1;
+                if constexpr (SK == SCALE_ROWCOL) {
+                    verdict = 0;   // unit block scales: the native path
+                } else if constexpr (SK == SCALE_TOKEN) {
+                    verdict = 1;   // per-row scales: the promotion path
+                } else if (c.mode != PATH_PROMOTE) {
+                    bool any_bad;
+                    if (i == 0) {
+                        any_bad = ctl->first_bad != 0;   // computed by warps 1..11 at the start
+                    } else {
+                        const Tile tt = sch.tile(unit + i * nunits);
+                        any_bad = __any_sync(FULL, tile_has_bad_scale<BN, C::TILE_M>(tt, sch.entry(tt.g), c, lane, 32));
+                    }
+                    verdict = any_bad ? 1 : 0;
+                    if (any_bad && c.mode == PATH_NATIVE && lane == 0) atomicOr(c.status, STATUS_SCALE);
+                }
+                if (lane == 0) {
+                    ctl->verdict[v] = verdict;
+                    mbar_arrive(&ctl->vfull[v]);
+                    trace_event(c, TR_VERDICT, i);
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
     } else if (warp == 3) {
         // --------------------------------------------------------- scale warp
@@ -1020,6 +1113,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         int bi = -1, bks = KW, bs = 0;
         uint32_t bph = 0;
         bool promote = false;
+        int bnb = NBB;   // per-row lines: column blocks of the build tile inside N
         bool ok = true;
         // each iteration first releases entry it - L, then issues entry it: the
         // release then finds no copy just issued still in flight
@@ -1032,6 +1126,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     ok = __all_sync(FULL, wait_bar(&ctl->vfull[v], static_cast<uint32_t>(bi >> 1) & 1u, ctl, c));
                     if (!ok) break;
                     promote = ctl->verdict[v] != 0;
+                    if constexpr (C::ROWA) bnb = min(NBB, c.N / 32 - sch.tile(unit + bi * nunits).n0 / 32);
                 }
                 if (lane == 0) trace_event(c, TR_SCALE_BUILD, it - L);
                 ok = __all_sync(FULL, wait_bar(&ctl->scfull[bs], bph, ctl, c));
@@ -1047,7 +1142,12 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         const float *sc = sm_sc + bs * C::SC_ENTRY + h * C::SC_FLOATS;
                         // (per-row / per-column scales: unit lines, 2^0)
                         const float va = (lane < 16 && SK == SCALE_BLOCK32) ? sc[(lane & 3) * 4 + (lane >> 2)] : 1.0f;
-                        const float vb = (lane < 4 * NBB && SK == SCALE_BLOCK32) ? sc[16 + (lane & 3) * NBB + (lane >> 2)] : 1.0f;
+                        const float vb = (lane < 4 * NBB && SK != SCALE_ROWCOL) ? sc[16 + (lane & 3) * NBB + (lane >> 2)] : 1.0f;
+                        // per-token native tiles have no verdict scan: B's block scales
+                        // inside the matrix are checked here
+                        if (C::ROWA && (lane >> 2) < bnb && (bks * H + h) * KB_PER_STAGE + (lane & 3) < c.KB &&
+                            !is_pow2_scale(vb))
+                            atomicOr(c.status, STATUS_SCALE);
                         wa[h] = ue8m0_of(va) << (8 * (lane & 3));
                         wb[h] = ue8m0_of(vb) << (8 * (lane & 3));
                     }
@@ -1069,7 +1169,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         la.y = __shfl_sync(FULL, wa[h], 4);
                         la.z = __shfl_sync(FULL, wa[h], 8);
                         la.w = __shfl_sync(FULL, wa[h], 12);
-                        if (lane < 8) *reinterpret_cast<uint4 *>(sf + lane * 16) = la;
+                        if (!C::ROWA && lane < 8) *reinterpret_cast<uint4 *>(sf + lane * 16) = la;   // (per-row lines: warp 2)
 #pragma unroll
                         for (int q = 0; q < C::SFB_CHUNKS; ++q) {
                             uint4 lb;
@@ -1077,7 +1177,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                             lb.y = __shfl_sync(FULL, wb[h], 16 * q + 4);
                             lb.z = __shfl_sync(FULL, wb[h], 16 * q + 8);
                             lb.w = __shfl_sync(FULL, wb[h], 16 * q + 12);
-                            if (lane < 8) *reinterpret_cast<uint4 *>(sf + C::SF_SET * (1 + q) + lane * 16) = lb;
+                            if (lane < 8) *reinterpret_cast<uint4 *>(sf + C::SF_SET_A + C::SF_SET * q + lane * 16) = lb;
                         }
                     }
                     // the lines become visible to tcgen05.cp's async-proxy reads

@@ -349,6 +349,16 @@ __device__ __forceinline__ uint64_t sdesc_sf_lines(uint32_t saddr) {
     return d;
 }
 
+// The same for 32 distinct 16-byte rows back to back (512 bytes): 8-row groups
+// 128 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sf_lines32(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128u >> 4) << 32;   // stride byte offset: 8 rows x 16 B
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+
 // Instruction descriptor, kind::f8f6f4: E4M3 x E4M3 -> fp32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t m, uint32_t n) {
     return (1u << 4)                 // D format: f32

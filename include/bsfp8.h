@@ -147,6 +147,20 @@ int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *
 int fp8_gemm_pertoken(const void *A, const float *sA, const void *B, const float *sB, void *C,
                       int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
+/* Same with an explicit path.  FP8_PATH_AUTO and FP8_PATH_PROMOTE: the
+ * promotion path above.  FP8_PATH_NATIVE: the block-scaled tensor-core path
+ * (kind::mxf8f6f4, UE8M0 scales) on CTA pairs with 256 x 256 tiles, each row
+ * of A carrying its own scale per 32-K block (1 x 32 scale vectors along K,
+ * the scale layout of MX formats), B its 32 x 32 blocks; every sA and sB
+ * value must be a positive normal power of two.  The scales are not scanned
+ * before the launch: a value that is not is reported as FP8_ERR_SCALE by
+ * fp8_status_query and the result is undefined.  Tiles and K order depend on
+ * N and K only, so each row's bits are the same for every M; the bits differ
+ * from the promotion path's (a different accumulation), both within the
+ * acceptance bound.  Returns as fp8_gemm_pertoken, or FP8_ERR_MODE. */
+int fp8_gemm_pertoken_ex(const void *A, const float *sA, const void *B, const float *sB, void *C,
+                         int64_t M, int64_t N, int64_t K, int mode, cudaStream_t stream);
+
 /* Block quantization of activations to the operand format above (FP8 GEMM
  * library article, hncyxsy.com/news/241433, section 2.1: E4M3, largest value
  * 448; section 2.2: one scale per 32x32 block).  For each 32x32 block of x:

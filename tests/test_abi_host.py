@@ -55,6 +55,21 @@ def test_shape_errors(lib):
     assert _call(lib, mode=7) == _abi.FP8_ERR_MODE
 
 
+def test_pertoken_argument_errors(lib):
+    def call(mode=0, **kw):
+        a = dict(A=16, sA=16, B=16, sB=16, C=16, M=64, N=64, K=64)
+        a.update(kw)
+        return lib.fp8_gemm_pertoken_ex(a["A"], a["sA"], a["B"], a["sB"], a["C"], a["M"], a["N"], a["K"], mode, None)
+    assert call(mode=7) == _abi.FP8_ERR_MODE
+    assert call(mode=-1) == _abi.FP8_ERR_MODE
+    assert call(N=33, mode=_abi.FP8_PATH_NATIVE) == _abi.FP8_ERR_SHAPE
+    assert call(K=48, mode=_abi.FP8_PATH_NATIVE) == _abi.FP8_ERR_SHAPE
+    assert call(C=0, mode=_abi.FP8_PATH_NATIVE) == _abi.FP8_ERR_NULL
+    assert call(C=8, mode=_abi.FP8_PATH_NATIVE) == _abi.FP8_ERR_ALIGN
+    assert call(sA=2, mode=_abi.FP8_PATH_NATIVE) == _abi.FP8_ERR_ALIGN
+    assert call(A=0, sA=0, B=0, sB=0, C=0, M=0, mode=_abi.FP8_PATH_NATIVE) == _abi.FP8_OK
+
+
 def test_empty_problems_enqueue_nothing(lib):
     # M == 0 or N == 0: OK without any device work (no device needed)
     assert _call(lib, A=0, sA=0, B=0, sB=0, C=0, M=0) == _abi.FP8_OK

@@ -103,3 +103,79 @@ def test_pertoken_square_4096_sampled(bs):
     Cr, T = oracle.gemm_pertoken(Ah[rows], sAh[rows], Bh, sBh, len(rows), N, K)   # whole rows
     Cg = C[torch.from_numpy(rows).to(DEV)]
     check(bf16_to_f64(Cg), Cr, T, "pertoken 4096^3 rows")
+
+
+# ------------------------------------------------------------- native path
+# FP8_PATH_NATIVE: power-of-two per-token scales on the block-scaled MMA, every
+# row of A with its own UE8M0 scale per 32-K block.
+
+def _run_native(bs, A, sA, B, sB, M, N, K):
+    buf = torch.full((M + 2, N), -7.0, dtype=torch.bfloat16, device=DEV)
+    C = buf[1:M + 1]
+    bs.fp8_gemm_pertoken(A.to(DEV), sA.to(DEV), B.to(DEV), sB.to(DEV), C, M, N, K, mode=bs.FP8_PATH_NATIVE)
+    torch.cuda.synchronize()
+    assert torch.all(buf[0] == -7.0) and torch.all(buf[-1] == -7.0), "store outside C"
+    return C
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (77, 256, 160), (256, 512, 1024), (300, 288, 2048),
+                                   (1000, 768, 1056)])
+def test_pertoken_native_parity(bs, M, N, K):
+    """Every row has its own scales (e uniform in [-4, 4] per row and K block):
+    a wrong row-to-line mapping would scale rows by other rows' factors.  K=160
+    and 1056 end inside a 128-K half; N=288 ends inside a 256-column tile."""
+    A, sA, B, sB = _problem(M, N, K, seed=11 * M + N + K, pow2=True)
+    C = _run_native(bs, A, sA, B, sB, M, N, K)
+    Cr, T = oracle.gemm_pertoken(A.numpy(), sA.numpy(), B.numpy(), sB.numpy(), M, N, K)
+    check(bf16_to_f64(C), Cr, T, f"pertoken native {M}x{N}x{K}")
+    assert bs.fp8_status_query() == 0
+
+
+def test_pertoken_native_block_constant_equals_block_scaled_native(bs):
+    """Scales equal within each 32-row block: the per-row lines hold the values
+    the block-scaled call replicates, so the two launches agree bit for bit."""
+    M, N, K = 1000, 512, 1024
+    A, _, B, sB = _problem(M, N, K, seed=12, pow2=True)
+    g = torch.Generator().manual_seed(13)
+    sA_blk = workloads.pow2_scales(M, K // 32, -4, 4, g, "cpu")   # [ceil(M/32), K/32]
+    assert sA_blk.shape == ((M + 31) // 32, K // 32)
+    sA_tok = sA_blk.repeat_interleave(32, dim=0)[:M].contiguous()
+    assert sA_tok.shape == (M, K // 32)
+    C_tok = _run_native(bs, A, sA_tok, B, sB, M, N, K)
+    C_blk = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    bs.fp8_gemm_blockscaled(A.to(DEV), sA_blk.to(DEV), B.to(DEV), sB.to(DEV), C_blk, M, N, K,
+                            mode=bs.FP8_PATH_NATIVE)
+    torch.cuda.synchronize()
+    assert bs.fp8_status_query() == 0
+    assert torch.equal(C_tok.view(torch.int16), C_blk.view(torch.int16))
+
+
+def test_pertoken_native_batch_invariance(bs):
+    M, N, K = 4096, 512, 1024
+    A, sA, B, sB = _problem(M, N, K, seed=14, pow2=True)
+    dB, dsB = B.to(DEV), sB.to(DEV)
+    rows = {}
+    for m in (1, 7, 64, M):
+        C = torch.empty(m, N, dtype=torch.bfloat16, device=DEV)
+        bs.fp8_gemm_pertoken(A[:m].contiguous().to(DEV), sA[:m].contiguous().to(DEV), dB, dsB, C, m, N, K,
+                             mode=bs.FP8_PATH_NATIVE)
+        torch.cuda.synchronize()
+        rows[m] = C[:min(m, 64)].cpu()
+    for m in (7, 64, M):
+        n = min(m, 64)
+        assert torch.equal(rows[m][:n].view(torch.int16), rows[M][:n].view(torch.int16)), m
+    assert torch.equal(rows[1].view(torch.int16), rows[M][:1].view(torch.int16))
+    assert bs.fp8_status_query() == 0
+
+
+@pytest.mark.parametrize("which", ["sA", "sB"])
+def test_pertoken_native_reports_a_scale_that_is_not_a_power_of_two(bs, which):
+    M, N, K = 300, 512, 1024
+    A, sA, B, sB = _problem(M, N, K, seed=15, pow2=True)
+    if which == "sA":
+        sA[137, 9] = 0.75
+    else:
+        sB[5, 30] = 3.0
+    _run_native(bs, A, sA, B, sB, M, N, K)
+    assert bs.fp8_status_query() == bs._abi.FP8_ERR_SCALE
+    assert bs.fp8_status_query() == 0   # the query clears the word
