@@ -981,66 +981,98 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             // For each scale-ring entry lane l writes line l of each 128-K half:
             // word w holds the UE8M0 scales of row 32w + l of this CTA's 128 rows,
             // byte j that of K block j of the half, so tcgen05.cp hands every row
-            // its own scales.  The scales of entry e + 1 are loaded (plain loads
-            // into registers) before entry e's lines are written; a scale that is
-            // not a positive normal power of two sets the status word's scale bit.
+            // its own scales.  The scales of entry e + 3 are loaded (plain loads
+            // into registers, four entries in flight: an L2 load under the
+            // operand traffic takes about as long as a stage) before entry e's
+            // lines are written; a scale that is not a positive normal power of
+            // two sets the status word's scale bit.
             // Every tile's verdict is the native path; it is published when the
             // lines reach the tile (the verdict of tile i waits only for tile i - 2).
             constexpr int H = C::HALVES;
             const int KW = (c.KS + H - 1) / H;
             const int total = my_tiles * KW;
-            auto load = [&](float (&dst)[H][16], int e) {
-                const int i = e / KW, ks = e - i * KW;
-                const Tile tt = sch.tile(unit + i * nunits);
-                const float *sa = sch.entry(tt.g).sA;
+            const bool vec = (c.KB & 3) == 0;   // rows of sA 16-byte aligned: one load per row and half
+            // load side: tile il, stage kl of the entry being loaded; this lane's
+            // four rows of that tile (null outside M)
+            int il = -1, kl = KW;
+            const float *lp[4] = {nullptr, nullptr, nullptr, nullptr};
+            auto load = [&](float (&dst)[H][16]) {
+                if (++kl >= KW) {
+                    kl = 0;
+                    ++il;
+                    const Tile tt = sch.tile(unit + il * nunits);
+                    const float *sa = sch.entry(tt.g).sA;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int row = tt.m0 + row_off + 32 * w + lane;
+                        lp[w] = row < tt.Mg ? sa + static_cast<int64_t>(row) * c.KB : nullptr;
+                    }
+                }
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    const int row = tt.m0 + row_off + 32 * w + lane;
-                    const bool rin = row < tt.Mg;
-                    const float *pr = sa + static_cast<int64_t>(rin ? row : 0) * c.KB;
 #pragma unroll
-                    for (int h = 0; h < H; ++h)
+                    for (int h = 0; h < H; ++h) {
+                        const int kb0 = (kl * H + h) * KB_PER_STAGE;
+                        if (vec) {
+                            const float4 q = (lp[w] != nullptr && kb0 < c.KB)
+                                                 ? __ldg(reinterpret_cast<const float4 *>(lp[w] + kb0))
+                                                 : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+                            dst[h][4 * w + 0] = q.x;
+                            dst[h][4 * w + 1] = q.y;
+                            dst[h][4 * w + 2] = q.z;
+                            dst[h][4 * w + 3] = q.w;
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < KB_PER_STAGE; ++j) {
-                            const int kb = (ks * H + h) * KB_PER_STAGE + j;
-                            dst[h][4 * w + j] = (rin && kb < c.KB) ? __ldg(pr + kb) : 1.0f;
+                            for (int j = 0; j < KB_PER_STAGE; ++j)
+                                dst[h][4 * w + j] =
+                                    (lp[w] != nullptr && kb0 + j < c.KB) ? __ldg(lp[w] + kb0 + j) : 1.0f;
                         }
+                    }
                 }
             };
-            auto build = [&](const float (&src)[H][16], int e) -> bool {
-                const int i = e / KW, ks = e - i * KW;
-                if (ks == 0) {
-                    const int v = i & 1;
-                    if (!__all_sync(FULL, wait_bar(&ctl->vempty[v], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u, ctl, c)))
+            // build side: tile ib, stage kbs, ring slot fb (phase phb)
+            int ib = -1, kbs = KW, fb = 0;
+            uint32_t phb = 0;
+            auto build = [&](const float (&src)[H][16]) -> bool {
+                if (++kbs >= KW) {
+                    kbs = 0;
+                    ++ib;
+                    const int v = ib & 1;
+                    if (!__all_sync(FULL, wait_bar(&ctl->vempty[v], (static_cast<uint32_t>(ib >> 1) & 1u) ^ 1u, ctl, c)))
                         return false;
                     if (lane == 0) {
                         ctl->verdict[v] = 0;
                         mbar_arrive(&ctl->vfull[v]);
-                        trace_event(c, TR_VERDICT, i);
+                        trace_event(c, TR_VERDICT, ib);
                     }
                     __syncwarp();
                 }
-                const int f = e % FS;
-                if (!__all_sync(FULL, wait_bar(&ctl->sfempty[f], (static_cast<uint32_t>(e / FS) & 1u) ^ 1u, ctl, c)))
-                    return false;
-                bool bad = false;
+                const int f = fb;
+                if (!__all_sync(FULL, wait_bar(&ctl->sfempty[f], phb ^ 1u, ctl, c))) return false;
+                if (++fb == FS) {
+                    fb = 0;
+                    phb ^= 1u;
+                }
+                // a positive normal power of two has sign and mantissa zero and
+                // 1 <= exponent <= 254; its UE8M0 byte is its exponent field, so
+                // a word of four is assembled by shifts alone
+                uint32_t mant = 0u, lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
                     uint32_t wd[4];
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
-                        uint32_t x = 0;
-#pragma unroll
-                        for (int j = 0; j < KB_PER_STAGE; ++j) {
-                            const float v = src[h][4 * w + j];
-                            bad |= !is_pow2_scale(v);
-                            x |= ue8m0_of(v) << (8 * j);
-                        }
-                        wd[w] = x;
+                        const uint32_t b0 = __float_as_uint(src[h][4 * w + 0]), b1 = __float_as_uint(src[h][4 * w + 1]);
+                        const uint32_t b2 = __float_as_uint(src[h][4 * w + 2]), b3 = __float_as_uint(src[h][4 * w + 3]);
+                        mant |= (b0 | b1 | b2 | b3) & 0x807FFFFFu;
+                        lo = min(lo, min(min(b0, b1), min(b2, b3)));
+                        hi = max(hi, max(max(b0, b1), max(b2, b3)));
+                        wd[w] = (b0 >> 23) | (b1 >> 15) | (b2 >> 7) | (b3 << 1);
                     }
                     *reinterpret_cast<uint4 *>(sm_sf + f * C::SF_ENTRY + h * C::SF_BYTES + lane * 16) =
                         make_uint4(wd[0], wd[1], wd[2], wd[3]);
                 }
+                const bool bad = mant != 0u || lo < 0x00800000u || hi >= 0x7F800000u;
                 if (__any_sync(FULL, bad) && lane == 0) atomicOr(c.status, STATUS_SCALE);
                 fence_proxy_async_smem();   // the lines become visible to tcgen05.cp
                 __syncwarp();
@@ -1048,13 +1080,19 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 __syncwarp();
                 return true;
             };
-            float ra[H][16], rb[H][16];
-            if (total > 0) load(ra, 0);
-            for (int e = 0; e < total; e += 2) {
-                if (e + 1 < total) load(rb, e + 1);
-                if (!build(ra, e) || e + 1 >= total) break;
-                if (e + 2 < total) load(ra, e + 2);
-                if (!build(rb, e + 1)) break;
+            float r0[H][16], r1[H][16], r2[H][16], r3[H][16];
+            if (total > 0) load(r0);
+            if (total > 1) load(r1);
+            if (total > 2) load(r2);
+            for (int e = 0; e < total; e += 4) {
+                if (e + 3 < total) load(r3);
+                if (!build(r0) || e + 1 >= total) break;
+                if (e + 4 < total) load(r0);
+                if (!build(r1) || e + 2 >= total) break;
+                if (e + 5 < total) load(r1);
+                if (!build(r2) || e + 3 >= total) break;
+                if (e + 6 < total) load(r2);
+                if (!build(r3)) break;
             }
         } else {
             // -------------------------------------------------------- path verdict
