@@ -991,10 +991,11 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             constexpr int H = C::HALVES;
             const int KW = (c.KS + H - 1) / H;
             const int total = my_tiles * KW;
-            const bool vec = (c.KB & 3) == 0;   // rows of sA 16-byte aligned: one load per row and half
             // load side: tile il, stage kl of the entry being loaded; this lane's
-            // four rows of that tile (null outside M)
+            // four rows of that tile (null outside M); vec: every row of sA
+            // starts on 16 bytes (the API promises only 4), one load per row and half
             int il = -1, kl = KW;
+            bool vec = false;
             const float *lp[4] = {nullptr, nullptr, nullptr, nullptr};
             auto load = [&](float (&dst)[H][16]) {
                 if (++kl >= KW) {
@@ -1002,6 +1003,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     ++il;
                     const Tile tt = sch.tile(unit + il * nunits);
                     const float *sa = sch.entry(tt.g).sA;
+                    vec = (c.KB & 3) == 0 && (reinterpret_cast<uintptr_t>(sa) & 15u) == 0;
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const int row = tt.m0 + row_off + 32 * w + lane;

@@ -179,3 +179,24 @@ def test_pertoken_native_reports_a_scale_that_is_not_a_power_of_two(bs, which):
     _run_native(bs, A, sA, B, sB, M, N, K)
     assert bs.fp8_status_query() == bs._abi.FP8_ERR_SCALE
     assert bs.fp8_status_query() == 0   # the query clears the word
+
+
+def test_pertoken_native_scales_only_4_byte_aligned(bs):
+    """sA and sB need only 4-byte alignment: scales starting 4 bytes into an
+    allocation give the same result as aligned copies, bit for bit."""
+    M, N, K = 300, 256, 1024
+    A, sA, B, sB = _problem(M, N, K, seed=16, pow2=True)
+    C_ref = _run_native(bs, A, sA, B, sB, M, N, K)
+    dA, dB = A.to(DEV), B.to(DEV)
+    bufA = torch.empty(sA.numel() + 1, dtype=torch.float32, device=DEV)
+    bufB = torch.empty(sB.numel() + 1, dtype=torch.float32, device=DEV)
+    sA_off = bufA[1:].view(sA.shape)
+    sB_off = bufB[1:].view(sB.shape)
+    sA_off.copy_(sA.to(DEV))
+    sB_off.copy_(sB.to(DEV))
+    assert sA_off.data_ptr() % 16 == 4 and sB_off.data_ptr() % 16 == 4
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    bs.fp8_gemm_pertoken(dA, sA_off, dB, sB_off, C, M, N, K, mode=bs.FP8_PATH_NATIVE)
+    torch.cuda.synchronize()
+    assert bs.fp8_status_query() == 0
+    assert torch.equal(C.view(torch.int16), C_ref.view(torch.int16))
