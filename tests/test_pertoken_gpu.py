@@ -200,3 +200,26 @@ def test_pertoken_native_scales_only_4_byte_aligned(bs):
     torch.cuda.synchronize()
     assert bs.fp8_status_query() == 0
     assert torch.equal(C.view(torch.int16), C_ref.view(torch.int16))
+
+
+def test_pertoken_native_square_4096_rows(bs):
+    """The bench's p1n shape (256 tiles on 76 CTA pairs, each pair running
+    several tiles, so the per-row scale pipeline crosses tile boundaries):
+    whole rows at tile edges and 60 random rows against the oracle."""
+    M = N = K = 4096
+    g = torch.Generator(device=DEV).manual_seed(9)
+    A = workloads.normal_codes(M, K, g, DEV)
+    B = workloads.normal_codes(N, K, g, DEV)
+    sA = torch.ldexp(torch.ones(M, K // 32, device=DEV),
+                     torch.randint(-4, 5, (M, K // 32), generator=g, device=DEV)).float()
+    sB = workloads.pow2_scales(N, K // 32, -4, 4, g, DEV)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    bs.fp8_gemm_pertoken(A, sA, B, sB, C, M, N, K, mode=bs.FP8_PATH_NATIVE)
+    torch.cuda.synchronize()
+    assert bs.fp8_status_query() == 0
+    rng = np.random.default_rng(9)
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, 2049, M - 1], rng.integers(0, M, 60)]))
+    Ah, sAh, Bh, sBh = (t.cpu().numpy() for t in (A, sA, B, sB))
+    Cr, T = oracle.gemm_pertoken(Ah[rows], sAh[rows], Bh, sBh, len(rows), N, K)   # whole rows
+    Cg = C[torch.from_numpy(rows).to(DEV)]
+    check(bf16_to_f64(Cg), Cr, T, "pertoken native 4096^3 rows")
