@@ -1010,6 +1010,17 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         lp[w] = row < tt.Mg ? sa + static_cast<int64_t>(row) * c.KB : nullptr;
                     }
                 }
+                // each row's next 128-byte line (the scales of the next four
+                // entries) goes to L1 ahead of its loads; one line ahead per row
+                // is 16 KB, what L1 holds beside this kernel's shared memory
+                if ((kl & 3) == 0) {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int nl = (kl >> 2) + 1;
+                        if (lp[w] != nullptr && nl * 32 < c.KB)
+                            asm volatile("prefetch.global.L1 [%0];" ::"l"(lp[w] + nl * 32));
+                    }
+                }
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
 #pragma unroll
