@@ -761,179 +761,179 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA warp
-        int it = 0;                       // 128-K steps consumed (the scale ring's sequence)
-        int ot = 0;                       // operand stages consumed (the producer's sequence)
-        const int KW = (c.KS + C::HALVES - 1) / C::HALVES;
-        uint32_t uses0 = 0, uses1 = 0;    // completed uses of tensor-memory buffers 0 / 1
-        uint32_t pk = 0;                  // promotion partials issued (buffer = pk & 1)
-        // Promotion tiles: the epilogue reads each K block's scales from the
-        // scale ring, so an entry is released (sfempty) only once the epilogue
-        // has read every partial of its stage.  The MMA warp learns that from
-        // its own tempty waits (the wait for partial p passes once partial p-2
-        // has been read); entries wait here, oldest first, with the index of
-        // their last partial.
-        int pend_f0 = -1, pend_l0 = 0, pend_f1 = -1, pend_l1 = 0;
-        // A pair's peer: in promotion tiles its epilogue releases a partial on
-        // its own barrier only, and this warp, which waits there anyway,
-        // forwards the release to the leader as one arrival counting for the
-        // peer's eight warps (bit b: buffer b's last use still to forward).
-        uint32_t fwd = 0;
-        auto forward_release = [&](uint32_t b) {
-            if (PAIR && !leader && ((fwd >> b) & 1u)) {
-                if (lane == 0) mbar_signal_cluster_count(mapa_shared(&ctl->tempty[b], 0), NUM_EPI_WARPS);
-                fwd &= ~(1u << b);
-            }
-        };
-        auto release_read = [&](int upto) {   // partials <= upto have been read
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                if (pend_f0 >= 0 && pend_l0 <= upto) {
-                    if (lane == 0) mbar_arrive(&ctl->sfempty[pend_f0]);
-                    pend_f0 = pend_f1;
-                    pend_l0 = pend_l1;
-                    pend_f1 = -1;
+        // One thread runs the role: the warp's other lanes wait at the end, so
+        // no tile boundary pays a warp-wide reconvergence.
+        if (lane == 0) {
+            int it = 0;                       // 128-K steps consumed (the scale ring's sequence)
+            int ot = 0;                       // operand stages consumed (the producer's sequence)
+            const int KW = (c.KS + C::HALVES - 1) / C::HALVES;
+            uint32_t uses0 = 0, uses1 = 0;    // completed uses of tensor-memory buffers 0 / 1
+            uint32_t pk = 0;                  // promotion partials issued (buffer = pk & 1)
+            // Promotion tiles: the epilogue reads each K block's scales from the
+            // scale ring, so an entry is released (sfempty) only once the epilogue
+            // has read every partial of its stage.  The MMA warp learns that from
+            // its own tempty waits (the wait for partial p passes once partial p-2
+            // has been read); entries wait here, oldest first, with the index of
+            // their last partial.
+            int pend_f0 = -1, pend_l0 = 0, pend_f1 = -1, pend_l1 = 0;
+            // A pair's peer: in promotion tiles its epilogue releases a partial on
+            // its own barrier only, and this warp, which waits there anyway,
+            // forwards the release to the leader as one arrival counting for the
+            // peer's eight warps (bit b: buffer b's last use still to forward).
+            uint32_t fwd = 0;
+            auto forward_release = [&](uint32_t b) {
+                if (PAIR && !leader && ((fwd >> b) & 1u)) {
+                    mbar_signal_cluster_count(mapa_shared(&ctl->tempty[b], 0), NUM_EPI_WARPS);
+                    fwd &= ~(1u << b);
                 }
-            }
-        };
-        bool ok = true;
-        bool issued = false;
-        for (int i = 0; i < my_tiles && ok; ++i) {
-            const int v = i & 1;
-            ok = __all_sync(FULL, wait_bar(&ctl->vfull[v], static_cast<uint32_t>(i >> 1) & 1u, ctl, c));
-            if (!ok) break;
-            const bool promote = ctl->verdict[v] != 0;
-            if (!promote && pend_f0 >= 0) {
-                // a promotion tile's last scale entries: both buffers drained
-                // means every partial has been read
-                ok = __all_sync(FULL, wait_bar(&ctl->tempty[0], (uses0 & 1u) ^ 1u, ctl, c) &&
-                                          wait_bar(&ctl->tempty[1], (uses1 & 1u) ^ 1u, ctl, c));
+            };
+            auto release_read = [&](int upto) {   // partials <= upto have been read
+    #pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if (pend_f0 >= 0 && pend_l0 <= upto) {
+                        mbar_arrive(&ctl->sfempty[pend_f0]);
+                        pend_f0 = pend_f1;
+                        pend_l0 = pend_l1;
+                        pend_f1 = -1;
+                    }
+                }
+            };
+            bool ok = true;
+            bool issued = false;
+            for (int i = 0; i < my_tiles && ok; ++i) {
+                const int v = i & 1;
+                ok = wait_spin(&ctl->vfull[v], static_cast<uint32_t>(i >> 1) & 1u, ctl, c);
                 if (!ok) break;
-                forward_release(0u);
-                forward_release(1u);
-                release_read(static_cast<int>(pk));
-            }
-            if (!promote) {
-                if (lane == 0 && leader) {
-                    trace_event(c, TR_MMA_VOK, i);
-                    // the accumulator (buffer 0) and, since the scale columns
-                    // share its range, buffer 1 must both be drained
-                    ok = wait_bar(&ctl->tempty[0], (uses0 & 1u) ^ 1u, ctl, c);
-                    trace_event(c, TR_MMA_T0, i);
-                    ok = ok && wait_bar(&ctl->tempty[1], (uses1 & 1u) ^ 1u, ctl, c);
-                    trace_event(c, TR_MMA_TILE, i);
-                    tc_fence_after();
-                    const uint32_t sfa_base = tmem + C::SF_COL0;
-                    // one pass per operand stage: the MMA pipe holds only about one
-                    // instruction, so the thread keeps the work between MMAs short
-                    // (counters instead of divisions; all scale copies of the stage
-                    // first, then its MMAs back to back)
-                    int s = ot % S, f = ot % FS;
-                    uint32_t ph = static_cast<uint32_t>(ot / S) & 1u, phf = static_cast<uint32_t>(ot / FS) & 1u;
-                    trace_event(c, TR_MMA_LOOP, i);
-                    // the next stage's barriers are tested (without blocking) just
-                    // before a stage's last MMA, whose issue waits for the pipe anyway
-                    bool next_ready = false;
-                    for (int w = 0; w < KW && ok; ++w) {
-                        if (!next_ready) {
-                            ok = wait_spin(&ctl->sfready[f], phf, ctl, c);
-                            trace_event(c, TR_MMA_SF_OK, ot + w);
-                            ok = ok && wait_spin(&ctl->full[s], ph, ctl, c);
-                            trace_event(c, TR_MMA_FULL_OK, ot + w);
-                            if (!ok) break;
-                        }
-                        next_ready = false;
-                        trace_event(c, TR_MMA_READY, ot + w);
-                        if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
+                const bool promote = ctl->verdict[v] != 0;
+                if (!promote && pend_f0 >= 0) {
+                    // a promotion tile's last scale entries: both buffers drained
+                    // means every partial has been read
+                    ok = wait_bar(&ctl->tempty[0], (uses0 & 1u) ^ 1u, ctl, c) &&
+                         wait_bar(&ctl->tempty[1], (uses1 & 1u) ^ 1u, ctl, c);
+                    if (!ok) break;
+                    forward_release(0u);
+                    forward_release(1u);
+                    release_read(static_cast<int>(pk));
+                }
+                if (!promote) {
+                    if (leader) {
+                        trace_event(c, TR_MMA_VOK, i);
+                        // the accumulator (buffer 0) and, since the scale columns
+                        // share its range, buffer 1 must both be drained
+                        ok = wait_spin(&ctl->tempty[0], (uses0 & 1u) ^ 1u, ctl, c);
+                        trace_event(c, TR_MMA_T0, i);
+                        ok = ok && wait_spin(&ctl->tempty[1], (uses1 & 1u) ^ 1u, ctl, c);
+                        trace_event(c, TR_MMA_TILE, i);
                         tc_fence_after();
-                        const uint32_t sfa = sfa_base + f * C::SF_ENTRY_COLS;
-                        const uint32_t sf_s = smem_u32(sm_sf + f * C::SF_ENTRY);
-                        const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
-                        const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
-                        const int nk = min(C::HALVES * KB_PER_STAGE, c.KB - w * C::HALVES * KB_PER_STAGE);
-#pragma unroll
-                        for (int hh = 0; hh < C::HALVES; ++hh) {
-                            if (hh * KB_PER_STAGE < nk) {
-                                cp_lines<PAIR>(sfa + hh * C::SF_COLS,
-                                               C::ROWA ? sdesc_sf_lines32(sf_s + hh * C::SF_BYTES)
-                                                       : sdesc_sf_lines(sf_s + hh * C::SF_BYTES));
-#pragma unroll
-                                for (int q = 0; q < C::SFB_CHUNKS; ++q)
-                                    cp_lines<PAIR>(sfa + hh * C::SF_COLS + 4 + 4 * q,
-                                                   sdesc_sf_lines(sf_s + hh * C::SF_BYTES + C::SF_SET_A + C::SF_SET * q));
+                        const uint32_t sfa_base = tmem + C::SF_COL0;
+                        // one pass per operand stage: the MMA pipe holds only about one
+                        // instruction, so the thread keeps the work between MMAs short
+                        // (counters instead of divisions; all scale copies of the stage
+                        // first, then its MMAs back to back)
+                        int s = ot % S, f = ot % FS;
+                        uint32_t ph = static_cast<uint32_t>(ot / S) & 1u, phf = static_cast<uint32_t>(ot / FS) & 1u;
+                        trace_event(c, TR_MMA_LOOP, i);
+                        // the next stage's barriers are tested (without blocking) just
+                        // before a stage's last MMA, whose issue waits for the pipe anyway
+                        bool next_ready = false;
+                        for (int w = 0; w < KW && ok; ++w) {
+                            if (!next_ready) {
+                                ok = wait_spin(&ctl->sfready[f], phf, ctl, c);
+                                trace_event(c, TR_MMA_SF_OK, ot + w);
+                                ok = ok && wait_spin(&ctl->full[s], ph, ctl, c);
+                                trace_event(c, TR_MMA_FULL_OK, ot + w);
+                                if (!ok) break;
                             }
-                        }
-#pragma unroll
-                        for (int hh = 0; hh < C::HALVES; ++hh) {
-#pragma unroll
-                            for (int j = 0; j < KB_PER_STAGE; ++j) {
-                                if (hh * KB_PER_STAGE + j < nk) {
-                                    if (hh == C::HALVES - 1 && j == KB_PER_STAGE - 1 && w + 1 < KW) {
-                                        const int s2 = s + 1 == S ? 0 : s + 1;
-                                        const int f2 = f + 1 == FS ? 0 : f + 1;
-                                        const uint32_t ph2 = s + 1 == S ? ph ^ 1u : ph;
-                                        const uint32_t phf2 = f + 1 == FS ? phf ^ 1u : phf;
-                                        next_ready = mbar_test_wait(&ctl->sfready[f2], phf2) &&
-                                                     mbar_test_wait(&ctl->full[s2], ph2);
-                                    }
-                                    mma_block<PAIR>(tmem, ad + static_cast<uint64_t>((hh * C::A_HALF >> 4) + 2 * j),
-                                                    bd + static_cast<uint64_t>((hh * C::B_HALF >> 4) + 2 * j),
-                                                    idesc_mxf8f6f4(C::MMA_M, BN, j, j), sfa + hh * C::SF_COLS,
-                                                    sfa + hh * C::SF_COLS + 4, (w | hh | j) != 0 ? 1u : 0u);
+                            next_ready = false;
+                            trace_event(c, TR_MMA_READY, ot + w);
+                            if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
+                            tc_fence_after();
+                            const uint32_t sfa = sfa_base + f * C::SF_ENTRY_COLS;
+                            const uint32_t sf_s = smem_u32(sm_sf + f * C::SF_ENTRY);
+                            const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
+                            const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
+                            const int nk = min(C::HALVES * KB_PER_STAGE, c.KB - w * C::HALVES * KB_PER_STAGE);
+    #pragma unroll
+                            for (int hh = 0; hh < C::HALVES; ++hh) {
+                                if (hh * KB_PER_STAGE < nk) {
+                                    cp_lines<PAIR>(sfa + hh * C::SF_COLS,
+                                                   C::ROWA ? sdesc_sf_lines32(sf_s + hh * C::SF_BYTES)
+                                                           : sdesc_sf_lines(sf_s + hh * C::SF_BYTES));
+    #pragma unroll
+                                    for (int q = 0; q < C::SFB_CHUNKS; ++q)
+                                        cp_lines<PAIR>(sfa + hh * C::SF_COLS + 4 + 4 * q,
+                                                       sdesc_sf_lines(sf_s + hh * C::SF_BYTES + C::SF_SET_A + C::SF_SET * q));
                                 }
                             }
+    #pragma unroll
+                            for (int hh = 0; hh < C::HALVES; ++hh) {
+    #pragma unroll
+                                for (int j = 0; j < KB_PER_STAGE; ++j) {
+                                    if (hh * KB_PER_STAGE + j < nk) {
+                                        if (hh == C::HALVES - 1 && j == KB_PER_STAGE - 1 && w + 1 < KW) {
+                                            const int s2 = s + 1 == S ? 0 : s + 1;
+                                            const int f2 = f + 1 == FS ? 0 : f + 1;
+                                            const uint32_t ph2 = s + 1 == S ? ph ^ 1u : ph;
+                                            const uint32_t phf2 = f + 1 == FS ? phf ^ 1u : phf;
+                                            next_ready = mbar_test_wait(&ctl->sfready[f2], phf2) &&
+                                                         mbar_test_wait(&ctl->full[s2], ph2);
+                                        }
+                                        mma_block<PAIR>(tmem, ad + static_cast<uint64_t>((hh * C::A_HALF >> 4) + 2 * j),
+                                                        bd + static_cast<uint64_t>((hh * C::B_HALF >> 4) + 2 * j),
+                                                        idesc_mxf8f6f4(C::MMA_M, BN, j, j), sfa + hh * C::SF_COLS,
+                                                        sfa + hh * C::SF_COLS + 4, (w | hh | j) != 0 ? 1u : 0u);
+                                    }
+                                }
+                            }
+                            commit_to<PAIR>(&ctl->empty[s]);
+                            commit_to<PAIR>(&ctl->sfempty[f]);
+                            trace_event(c, TR_MMA_ISSUED, ot + w);
+                            issued = true;
+                            if (++s == S) { s = 0; ph ^= 1u; }
+                            if (++f == FS) { f = 0; phf ^= 1u; }
                         }
-                        commit_to<PAIR>(&ctl->empty[s]);
-                        commit_to<PAIR>(&ctl->sfempty[f]);
-                        trace_event(c, TR_MMA_ISSUED, ot + w);
-                        issued = true;
-                        if (++s == S) { s = 0; ph ^= 1u; }
-                        if (++f == FS) { f = 0; phf ^= 1u; }
+                        if (ok) commit_to<PAIR>(&ctl->tfull[0]);
                     }
-                    if (ok) commit_to<PAIR>(&ctl->tfull[0]);
-                }
-                if (PAIR && !leader && lane == 0) {
-                    // forward each stage's scale lines to the leader's MMA thread
-                    for (int w = 0; w < KW && ok; ++w) {
-                        const int os = ot + w;
-                        const int f = os % FS;
-                        ok = wait_spin(&ctl->sfready[f], static_cast<uint32_t>(os / FS) & 1u, ctl, c);
-                        if (ok) mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
-                        trace_event(c, TR_PEER_FWD, os);
+                    if (PAIR && !leader) {
+                        // forward each stage's scale lines to the leader's MMA thread
+                        for (int w = 0; w < KW && ok; ++w) {
+                            const int os = ot + w;
+                            const int f = os % FS;
+                            ok = wait_spin(&ctl->sfready[f], static_cast<uint32_t>(os / FS) & 1u, ctl, c);
+                            if (ok) mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
+                            trace_event(c, TR_PEER_FWD, os);
+                        }
                     }
-                }
-                ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
-                issued = __shfl_sync(FULL, issued ? 1 : 0, 0) != 0;
-                if (!ok) break;
-                it += c.KS;
-                ot += KW;
-                ++uses0;
-            } else {
-                if (pk & 1u) ++pk;   // promotion tiles start on buffer 0 (see the header)
-                for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
-                    const int os = ot + ks / C::HALVES;   // operand stage and scale entry; half hh of it
-                    const int hh = ks % C::HALVES;
-                    const bool stage_done = hh == C::HALVES - 1 || ks == c.KS - 1;
-                    const int s = os % S;
-                    const int f = os % FS;
-                    const uint32_t phs = static_cast<uint32_t>(os / S) & 1u;
-                    ok = __all_sync(FULL, (PAIR && !leader ? true : wait_bar(&ctl->full[s], phs, ctl, c)) &&
-                                              wait_bar(&ctl->sfready[f], static_cast<uint32_t>(os / FS) & 1u, ctl, c));
                     if (!ok) break;
-                    if (PAIR && !leader && lane == 0 && hh == 0) {
-                        mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
-                    }
-                    if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
-                    const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES + hh * C::A_HALF));
-                    const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES + hh * C::B_HALF));
-                    const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
-                    for (int j = 0; j < nk; ++j) {
-                        const uint32_t b = pk & 1u;
-                        const uint32_t ub = b ? uses1 : uses0;
-                        ok = __all_sync(FULL, wait_bar(&ctl->tempty[b], (ub & 1u) ^ 1u, ctl, c));
+                    it += c.KS;
+                    ot += KW;
+                    ++uses0;
+                } else {
+                    if (pk & 1u) ++pk;   // promotion tiles start on buffer 0 (see the header)
+                    for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
+                        const int os = ot + ks / C::HALVES;   // operand stage and scale entry; half hh of it
+                        const int hh = ks % C::HALVES;
+                        const bool stage_done = hh == C::HALVES - 1 || ks == c.KS - 1;
+                        const int s = os % S;
+                        const int f = os % FS;
+                        const uint32_t phs = static_cast<uint32_t>(os / S) & 1u;
+                        ok = (PAIR && !leader ? true : wait_bar(&ctl->full[s], phs, ctl, c)) &&
+                             wait_bar(&ctl->sfready[f], static_cast<uint32_t>(os / FS) & 1u, ctl, c);
                         if (!ok) break;
-                        forward_release(b);
-                        release_read(static_cast<int>(pk) - 2);
-                        if (lane == 0) {
+                        if (PAIR && !leader && hh == 0) {
+                            mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
+                        }
+                        if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
+                        const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES + hh * C::A_HALF));
+                        const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES + hh * C::B_HALF));
+                        const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
+                        for (int j = 0; j < nk; ++j) {
+                            const uint32_t b = pk & 1u;
+                            const uint32_t ub = b ? uses1 : uses0;
+                            ok = wait_bar(&ctl->tempty[b], (ub & 1u) ^ 1u, ctl, c);
+                            if (!ok) break;
+                            forward_release(b);
+                            release_read(static_cast<int>(pk) - 2);
                             if (leader) {
                                 tc_fence_after();
                                 if constexpr (PAIR) {
@@ -946,32 +946,30 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                                     mma_commit(&ctl->tfull[b]);
                                 }
                             }
+                            issued = true;
+                            if (b) ++uses1; else ++uses0;
+                            fwd |= 1u << b;
+                            ++pk;
                         }
-                        issued = true;
-                        if (b) ++uses1; else ++uses0;
-                        fwd |= 1u << b;
-                        ++pk;
+                        if (!ok) break;
+                        if (stage_done) {
+                            if (leader) commit_to<PAIR>(&ctl->empty[s]);
+                            // the stage's scale entry, released once its partials are read
+                            if (pend_f0 < 0) { pend_f0 = f; pend_l0 = static_cast<int>(pk) - 1; }
+                            else { pend_f1 = f; pend_l1 = static_cast<int>(pk) - 1; }
+                        }
                     }
                     if (!ok) break;
-                    if (stage_done) {
-                        if (lane == 0 && leader) commit_to<PAIR>(&ctl->empty[s]);
-                        // the stage's scale entry, released once its partials are read
-                        if (pend_f0 < 0) { pend_f0 = f; pend_l0 = static_cast<int>(pk) - 1; }
-                        else { pend_f1 = f; pend_l1 = static_cast<int>(pk) - 1; }
-                    }
-                    __syncwarp();
+                    ot += KW;
                 }
-                if (!ok) break;
-                ot += KW;
+                mbar_arrive(&ctl->vempty[v]);
             }
-            if (lane == 0) mbar_arrive(&ctl->vempty[v]);
-            __syncwarp();
-        }
-        // all issued tensor-core work must finish before tensor memory is freed
-        if (issued && lane == 0 && leader) {
-            if constexpr (PAIR) mma_commit_pair(&ctl->drain, 0x1);
-            else mma_commit(&ctl->drain);
-            wait_bar_drain(&ctl->drain, 0u, c.wait_limit);
+            // all issued tensor-core work must finish before tensor memory is freed
+            if (issued && leader) {
+                if constexpr (PAIR) mma_commit_pair(&ctl->drain, 0x1);
+                else mma_commit(&ctl->drain);
+                wait_bar_drain(&ctl->drain, 0u, c.wait_limit);
+            }
         }
         __syncwarp();
     } else if (warp == 2) {
