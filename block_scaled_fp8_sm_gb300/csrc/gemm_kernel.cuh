@@ -170,14 +170,15 @@ struct Common {
 };
 
 // Event trace (profiling aid, off when the pointer is null): CTA 0 records the
-// SM clock of pipeline events into trace[event * TRACE_SLOTS + index].
+// SM clock of pipeline events into trace[event * TRACE_SLOTS + index].  The
+// MMA thread records per-tile events only: a test of the trace pointer between
+// a stage's MMAs costs ~3 % of the prefill GEMM (events 3, 4, 13 and 14 are
+// unused).
 constexpr int TRACE_SLOTS = 1024;
 enum : int {
     TR_PROD_ISSUE = 0,      // producer: slot free, issuing stage `it`
     TR_SCALE_FULL = 1,      // scale warp: stage `it` landed
     TR_SCALE_READY = 2,     // scale warp: stage `it` lines written, released
-    TR_MMA_READY = 3,       // MMA lane 0: stage `it` available
-    TR_MMA_ISSUED = 4,      // MMA lane 0: stage `it` MMAs issued and committed
     TR_EPI_FULL = 5,        // epilogue warp 4: accumulator of tile `i` ready
     TR_EPI_RELEASED = 6,    // epilogue warp 4: accumulator of tile `i` released
     TR_EPI_STORED = 7,      // epilogue warp 4: tile `i` stored
@@ -186,8 +187,6 @@ enum : int {
     TR_PROD_TMA = 10,       // producer: stage `it` TMA issued
     TR_SCALE_ISSUE = 11,    // scale warp: entry free, issuing the copies of step `it`
     TR_SCALE_BUILD = 12,    // scale warp: starting step `it`'s lines (before waiting for its copies)
-    TR_MMA_SF_OK = 13,      // MMA lane 0: scale lines of stage `it` ready
-    TR_MMA_FULL_OK = 14,    // MMA lane 0: own operand bytes of stage `it` landed
     TR_PEER_FWD = 15,       // peer MMA warp: its scale lines of stage `it` forwarded
     TR_MMA_VOK = 16,        // MMA lane 0: verdict of tile `i` seen
     TR_MMA_T0 = 17,         // MMA lane 0: accumulator released by the local epilogue (tile `i`)
@@ -524,6 +523,38 @@ __device__ __forceinline__ void commit_to(uint64_t *bar) {
     else mma_commit(bar);
 }
 
+// The scale copies and block-scaled MMAs of one operand stage (nk of its K
+// blocks present; acc0: the stage's first MMA accumulates).  FULL stages are
+// issued as one straight line: the tensor pipe holds about one MMA, so a
+// branch between two MMAs delays the second one's issue past the first one's
+// end (a full stage measured ~5 % faster on the prefill GEMM without them).
+template <typename C, bool FULL>
+__device__ __forceinline__ void issue_native_stage(uint32_t tmem, uint32_t sfa, uint32_t sf_s, uint64_t ad,
+                                                   uint64_t bd, int nk, uint32_t acc0) {
+#pragma unroll
+    for (int hh = 0; hh < C::HALVES; ++hh) {
+        if (FULL || hh * KB_PER_STAGE < nk) {
+            cp_lines<C::PAIR>(sfa + hh * C::SF_COLS, C::ROWA ? sdesc_sf_lines32(sf_s + hh * C::SF_BYTES)
+                                                             : sdesc_sf_lines(sf_s + hh * C::SF_BYTES));
+#pragma unroll
+            for (int q = 0; q < C::SFB_CHUNKS; ++q)
+                cp_lines<C::PAIR>(sfa + hh * C::SF_COLS + 4 + 4 * q,
+                                  sdesc_sf_lines(sf_s + hh * C::SF_BYTES + C::SF_SET_A + C::SF_SET * q));
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < C::HALVES; ++hh) {
+#pragma unroll
+        for (int j = 0; j < KB_PER_STAGE; ++j) {
+            if (FULL || hh * KB_PER_STAGE + j < nk)
+                mma_block<C::PAIR>(tmem, ad + static_cast<uint64_t>((hh * C::A_HALF >> 4) + 2 * j),
+                                   bd + static_cast<uint64_t>((hh * C::B_HALF >> 4) + 2 * j),
+                                   idesc_mxf8f6f4(C::MMA_M, C::BN, j, j), sfa + hh * C::SF_COLS,
+                                   sfa + hh * C::SF_COLS + 4, (hh | j) != 0 ? 1u : acc0);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // SK: scale layout; RES: a bf16 residual is added before the bf16 rounding.
 template <int BN, bool GROUPED, bool PAIR, typename Args, int SK = SCALE_BLOCK32, bool RES = false>
@@ -788,7 +819,7 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 }
             };
             auto release_read = [&](int upto) {   // partials <= upto have been read
-    #pragma unroll
+#pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     if (pend_f0 >= 0 && pend_l0 <= upto) {
                         mbar_arrive(&ctl->sfempty[pend_f0]);
@@ -829,23 +860,18 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         // one pass per operand stage: the MMA pipe holds only about one
                         // instruction, so the thread keeps the work between MMAs short
                         // (counters instead of divisions; all scale copies of the stage
-                        // first, then its MMAs back to back)
+                        // first, then its MMAs back to back; no trace events here)
                         int s = ot % S, f = ot % FS;
                         uint32_t ph = static_cast<uint32_t>(ot / S) & 1u, phf = static_cast<uint32_t>(ot / FS) & 1u;
                         trace_event(c, TR_MMA_LOOP, i);
-                        // the next stage's barriers are tested (without blocking) just
-                        // before a stage's last MMA, whose issue waits for the pipe anyway
+                        // the next stage's barriers are tested (without blocking) right
+                        // after a stage's commits, while its last MMA still runs
                         bool next_ready = false;
                         for (int w = 0; w < KW && ok; ++w) {
                             if (!next_ready) {
-                                ok = wait_spin(&ctl->sfready[f], phf, ctl, c);
-                                trace_event(c, TR_MMA_SF_OK, ot + w);
-                                ok = ok && wait_spin(&ctl->full[s], ph, ctl, c);
-                                trace_event(c, TR_MMA_FULL_OK, ot + w);
+                                ok = wait_spin(&ctl->sfready[f], phf, ctl, c) && wait_spin(&ctl->full[s], ph, ctl, c);
                                 if (!ok) break;
                             }
-                            next_ready = false;
-                            trace_event(c, TR_MMA_READY, ot + w);
                             if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
                             tc_fence_after();
                             const uint32_t sfa = sfa_base + f * C::SF_ENTRY_COLS;
@@ -853,44 +879,21 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                             const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
                             const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
                             const int nk = min(C::HALVES * KB_PER_STAGE, c.KB - w * C::HALVES * KB_PER_STAGE);
-    #pragma unroll
-                            for (int hh = 0; hh < C::HALVES; ++hh) {
-                                if (hh * KB_PER_STAGE < nk) {
-                                    cp_lines<PAIR>(sfa + hh * C::SF_COLS,
-                                                   C::ROWA ? sdesc_sf_lines32(sf_s + hh * C::SF_BYTES)
-                                                           : sdesc_sf_lines(sf_s + hh * C::SF_BYTES));
-    #pragma unroll
-                                    for (int q = 0; q < C::SFB_CHUNKS; ++q)
-                                        cp_lines<PAIR>(sfa + hh * C::SF_COLS + 4 + 4 * q,
-                                                       sdesc_sf_lines(sf_s + hh * C::SF_BYTES + C::SF_SET_A + C::SF_SET * q));
-                                }
-                            }
-    #pragma unroll
-                            for (int hh = 0; hh < C::HALVES; ++hh) {
-    #pragma unroll
-                                for (int j = 0; j < KB_PER_STAGE; ++j) {
-                                    if (hh * KB_PER_STAGE + j < nk) {
-                                        if (hh == C::HALVES - 1 && j == KB_PER_STAGE - 1 && w + 1 < KW) {
-                                            const int s2 = s + 1 == S ? 0 : s + 1;
-                                            const int f2 = f + 1 == FS ? 0 : f + 1;
-                                            const uint32_t ph2 = s + 1 == S ? ph ^ 1u : ph;
-                                            const uint32_t phf2 = f + 1 == FS ? phf ^ 1u : phf;
-                                            next_ready = mbar_test_wait(&ctl->sfready[f2], phf2) &&
-                                                         mbar_test_wait(&ctl->full[s2], ph2);
-                                        }
-                                        mma_block<PAIR>(tmem, ad + static_cast<uint64_t>((hh * C::A_HALF >> 4) + 2 * j),
-                                                        bd + static_cast<uint64_t>((hh * C::B_HALF >> 4) + 2 * j),
-                                                        idesc_mxf8f6f4(C::MMA_M, BN, j, j), sfa + hh * C::SF_COLS,
-                                                        sfa + hh * C::SF_COLS + 4, (w | hh | j) != 0 ? 1u : 0u);
-                                    }
-                                }
-                            }
+                            const uint32_t acc0 = w != 0 ? 1u : 0u;
+                            // (per-token lines keep the guarded body: their stages wait for
+                            // warp 2's scale loads, and the straight line measured 2-3 %
+                            // slower there)
+                            if (!C::ROWA && nk == C::HALVES * KB_PER_STAGE)
+                                issue_native_stage<C, true>(tmem, sfa, sf_s, ad, bd, nk, acc0);
+                            else
+                                issue_native_stage<C, false>(tmem, sfa, sf_s, ad, bd, nk, acc0);
                             commit_to<PAIR>(&ctl->empty[s]);
                             commit_to<PAIR>(&ctl->sfempty[f]);
-                            trace_event(c, TR_MMA_ISSUED, ot + w);
                             issued = true;
                             if (++s == S) { s = 0; ph ^= 1u; }
                             if (++f == FS) { f = 0; phf ^= 1u; }
+                            next_ready = w + 1 < KW && mbar_test_wait(&ctl->sfready[f], phf) &&
+                                         mbar_test_wait(&ctl->full[s], ph);
                         }
                         if (ok) commit_to<PAIR>(&ctl->tfull[0]);
                     }
