@@ -73,6 +73,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -864,37 +865,44 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         int s = ot % S, f = ot % FS;
                         uint32_t ph = static_cast<uint32_t>(ot / S) & 1u, phf = static_cast<uint32_t>(ot / FS) & 1u;
                         trace_event(c, TR_MMA_LOOP, i);
-                        // the next stage's barriers are tested (without blocking) right
-                        // after a stage's commits, while its last MMA still runs
+                        // One operand stage: its barriers (unless the previous stage found
+                        // them complete), scale copies and MMAs, commits; then the next
+                        // stage's barriers are tested (without blocking, one test of both,
+                        // no branch) while the last MMA still runs.  Each branch of this
+                        // single thread costs tens of cycles in which the pipe may run dry.
                         bool next_ready = false;
-                        for (int w = 0; w < KW && ok; ++w) {
-                            if (!next_ready) {
-                                ok = wait_spin(&ctl->sfready[f], phf, ctl, c) && wait_spin(&ctl->full[s], ph, ctl, c);
-                                if (!ok) break;
-                            }
+                        auto stage = [&](auto full, int w) -> bool {
+                            if (!next_ready &&
+                                !(wait_spin(&ctl->sfready[f], phf, ctl, c) && wait_spin(&ctl->full[s], ph, ctl, c)))
+                                return false;
                             if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
                             tc_fence_after();
                             const uint32_t sfa = sfa_base + f * C::SF_ENTRY_COLS;
                             const uint32_t sf_s = smem_u32(sm_sf + f * C::SF_ENTRY);
                             const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
                             const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
-                            const int nk = min(C::HALVES * KB_PER_STAGE, c.KB - w * C::HALVES * KB_PER_STAGE);
-                            const uint32_t acc0 = w != 0 ? 1u : 0u;
-                            // (per-token lines keep the guarded body: their stages wait for
-                            // warp 2's scale loads, and the straight line measured 2-3 %
-                            // slower there)
-                            if (!C::ROWA && nk == C::HALVES * KB_PER_STAGE)
-                                issue_native_stage<C, true>(tmem, sfa, sf_s, ad, bd, nk, acc0);
-                            else
-                                issue_native_stage<C, false>(tmem, sfa, sf_s, ad, bd, nk, acc0);
+                            const int nk = decltype(full)::value ? C::HALVES * KB_PER_STAGE
+                                                                 : min(C::HALVES * KB_PER_STAGE, c.KB - w * C::HALVES * KB_PER_STAGE);
+                            issue_native_stage<C, decltype(full)::value>(tmem, sfa, sf_s, ad, bd, nk, w != 0 ? 1u : 0u);
                             commit_to<PAIR>(&ctl->empty[s]);
                             commit_to<PAIR>(&ctl->sfempty[f]);
-                            issued = true;
-                            if (++s == S) { s = 0; ph ^= 1u; }
-                            if (++f == FS) { f = 0; phf ^= 1u; }
-                            next_ready = w + 1 < KW && mbar_test_wait(&ctl->sfready[f], phf) &&
-                                         mbar_test_wait(&ctl->full[s], ph);
-                        }
+                            s = s + 1 == S ? 0 : s + 1;
+                            ph ^= s == 0 ? 1u : 0u;
+                            f = f + 1 == FS ? 0 : f + 1;
+                            phf ^= f == 0 ? 1u : 0u;
+                            next_ready = mbar_test_wait2(&ctl->sfready[f], phf, &ctl->full[s], ph) & (w + 1 < KW);
+                            return true;
+                        };
+                        // Full stages first, as straight lines of copies and MMAs; a
+                        // partial last stage (K not a multiple of 256) after them.  Per-token
+                        // lines keep the guarded body for every stage: their stages wait
+                        // for warp 2's scale loads, and the straight line measured 2-3 %
+                        // slower there.
+                        const int kw_full = C::ROWA ? 0 : c.KB / (C::HALVES * KB_PER_STAGE);
+                        int w = 0;
+                        for (; w < kw_full && ok; ++w) ok = stage(std::true_type{}, w);
+                        for (; w < KW && ok; ++w) ok = stage(std::false_type{}, w);
+                        issued = issued || KW > 0;
                         if (ok) commit_to<PAIR>(&ctl->tfull[0]);
                     }
                     if (PAIR && !leader) {

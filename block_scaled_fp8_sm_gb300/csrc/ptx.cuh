@@ -70,6 +70,22 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0u;
 }
 
+// Two non-blocking phase tests in one block: both loads are in flight together,
+// and the result is whether both phases have completed.
+__device__ __forceinline__ bool mbar_test_wait2(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+        "and.pred p, p, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1)
+        : "memory");
+    return ok != 0u;
+}
+
 // Non-blocking test of phase `parity` (never suspends the thread).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
