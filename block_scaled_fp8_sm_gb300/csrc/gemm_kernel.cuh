@@ -1328,6 +1328,17 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             const bool row_ok = row < tt.Mg && 32 * q + lane < C::TILE_M;
             const int col0 = h * C::EPI_COLS;
             __nv_bfloat16 *crow = e.C + static_cast<int64_t>(row_ok ? row : 0) * c.N + tt.n0;
+            if constexpr (RES) {
+                // this thread's 256 bytes of the residual row into L2 while the
+                // tile's K loop runs: the chunk loads of the epilogue (and the
+                // last tile's, which nothing overlaps) then hit L2 (+1 % on the
+                // 4096^3 GEMM with a residual)
+                if (row_ok) {
+                    const __nv_bfloat16 *rr = args.R + static_cast<int64_t>(row) * c.N + tt.n0 + col0;
+                    if (tt.n0 + col0 < c.N) prefetch_l2(rr);
+                    if (tt.n0 + col0 + 64 < c.N) prefetch_l2(rr + 64);
+                }
+            }
 
             if (!promote) {
                 ok = __all_sync(FULL, wait_poll(&ctl->tfull[0], uses0 & 1u, ctl, c));

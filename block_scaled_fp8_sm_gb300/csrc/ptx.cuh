@@ -70,6 +70,12 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0u;
 }
 
+// Hint: bring the 128-byte line holding p into L2 (no result; callers pass
+// addresses inside their buffers).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Two non-blocking phase tests in one block: both loads are in flight together,
 // and the result is whether both phases have completed.
 __device__ __forceinline__ bool mbar_test_wait2(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1) {
