@@ -796,7 +796,6 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         // One thread runs the role: the warp's other lanes wait at the end, so
         // no tile boundary pays a warp-wide reconvergence.
         if (lane == 0) {
-            int it = 0;                       // 128-K steps consumed (the scale ring's sequence)
             int ot = 0;                       // operand stages consumed (the producer's sequence)
             const int KW = (c.KS + C::HALVES - 1) / C::HALVES;
             uint32_t uses0 = 0, uses1 = 0;    // completed uses of tensor-memory buffers 0 / 1
@@ -916,44 +915,37 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         }
                     }
                     if (!ok) break;
-                    it += c.KS;
                     ot += KW;
                     ++uses0;
                 } else {
                     if (pk & 1u) ++pk;   // promotion tiles start on buffer 0 (see the header)
-                    for (int ks = 0; ks < c.KS && ok; ++ks, ++it) {
-                        const int os = ot + ks / C::HALVES;   // operand stage and scale entry; half hh of it
-                        const int hh = ks % C::HALVES;
-                        const bool stage_done = hh == C::HALVES - 1 || ks == c.KS - 1;
-                        const int s = os % S;
-                        const int f = os % FS;
-                        const uint32_t phs = static_cast<uint32_t>(os / S) & 1u;
-                        ok = (PAIR && !leader ? true : wait_bar(&ctl->full[s], phs, ctl, c)) &&
-                             wait_bar(&ctl->sfready[f], static_cast<uint32_t>(os / FS) & 1u, ctl, c);
+                    int s = ot % S, f = ot % FS;
+                    uint32_t ph = static_cast<uint32_t>(ot / S) & 1u, phf = static_cast<uint32_t>(ot / FS) & 1u;
+                    const int kw_full = c.KB / (C::HALVES * KB_PER_STAGE);
+                    for (int w = 0; w < KW && ok; ++w) {
+                        ok = (PAIR && !leader ? true : wait_bar(&ctl->full[s], ph, ctl, c)) &&
+                             wait_bar(&ctl->sfready[f], phf, ctl, c);
                         if (!ok) break;
-                        if (PAIR && !leader && hh == 0) {
-                            mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
-                        }
+                        if (PAIR && !leader) mbar_signal_cluster(mapa_shared(&ctl->sfready[f], 0));
                         if constexpr (GROUPED) fence_proxy_async_smem();   // A rows written by cp.async
-                        const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES + hh * C::A_HALF));
-                        const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES + hh * C::B_HALF));
-                        const int nk = min(KB_PER_STAGE, c.KB - ks * KB_PER_STAGE);
-                        for (int j = 0; j < nk; ++j) {
-                            const uint32_t b = pk & 1u;
-                            const uint32_t ub = b ? uses1 : uses0;
-                            ok = wait_bar(&ctl->tempty[b], (ub & 1u) ^ 1u, ctl, c);
-                            if (!ok) break;
+                        const uint64_t ad = sdesc_k_sw128(smem_u32(sm_a + s * C::A_BYTES));
+                        const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
+                        // partial j of the stage (K block j % 4 of half j / 4) into buffer b,
+                        // once the epilogue has read that buffer's previous partial
+                        auto partial = [&](int j, uint32_t b) -> bool {
+                            if (!wait_bar(&ctl->tempty[b], ((b ? uses1 : uses0) & 1u) ^ 1u, ctl, c)) return false;
                             forward_release(b);
                             release_read(static_cast<int>(pk) - 2);
                             if (leader) {
+                                const int hh = j / KB_PER_STAGE, jj = j % KB_PER_STAGE;
+                                const uint64_t a_j = ad + static_cast<uint64_t>((hh * C::A_HALF >> 4) + 2 * jj);
+                                const uint64_t b_j = bd + static_cast<uint64_t>((hh * C::B_HALF >> 4) + 2 * jj);
                                 tc_fence_after();
                                 if constexpr (PAIR) {
-                                    mma_f8_pair(tmem + b * BN, ad + static_cast<uint64_t>(2 * j),
-                                                bd + static_cast<uint64_t>(2 * j), idesc_f8f6f4(C::MMA_M, BN), 0u);
+                                    mma_f8_pair(tmem + b * BN, a_j, b_j, idesc_f8f6f4(C::MMA_M, BN), 0u);
                                     mma_commit_pair(&ctl->tfull[b], PAIR_MASK);
                                 } else {
-                                    mma_f8(tmem + b * BN, ad + static_cast<uint64_t>(2 * j),
-                                           bd + static_cast<uint64_t>(2 * j), idesc_f8f6f4(BM, BN), 0u);
+                                    mma_f8(tmem + b * BN, a_j, b_j, idesc_f8f6f4(BM, BN), 0u);
                                     mma_commit(&ctl->tfull[b]);
                                 }
                             }
@@ -961,14 +953,27 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                             if (b) ++uses1; else ++uses0;
                             fwd |= 1u << b;
                             ++pk;
+                            return true;
+                        };
+                        if (w < kw_full) {
+                            // a full stage: an even number of partials from an even pk, so
+                            // partial j uses buffer j & 1 (known when the loop is unrolled)
+#pragma unroll
+                            for (int j = 0; j < C::HALVES * KB_PER_STAGE; ++j)
+                                if (ok) ok = partial(j, static_cast<uint32_t>(j & 1));
+                        } else {
+                            const int nk = c.KB - w * C::HALVES * KB_PER_STAGE;
+                            for (int j = 0; j < nk && ok; ++j) ok = partial(j, pk & 1u);
                         }
                         if (!ok) break;
-                        if (stage_done) {
-                            if (leader) commit_to<PAIR>(&ctl->empty[s]);
-                            // the stage's scale entry, released once its partials are read
-                            if (pend_f0 < 0) { pend_f0 = f; pend_l0 = static_cast<int>(pk) - 1; }
-                            else { pend_f1 = f; pend_l1 = static_cast<int>(pk) - 1; }
-                        }
+                        if (leader) commit_to<PAIR>(&ctl->empty[s]);
+                        // the stage's scale entry, released once its partials are read
+                        if (pend_f0 < 0) { pend_f0 = f; pend_l0 = static_cast<int>(pk) - 1; }
+                        else { pend_f1 = f; pend_l1 = static_cast<int>(pk) - 1; }
+                        s = s + 1 == S ? 0 : s + 1;
+                        ph ^= s == 0 ? 1u : 0u;
+                        f = f + 1 == FS ? 0 : f + 1;
+                        phf ^= f == 0 ? 1u : 0u;
                     }
                     if (!ok) break;
                     ot += KW;
