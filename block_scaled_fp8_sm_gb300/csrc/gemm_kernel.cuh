@@ -802,13 +802,13 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             uint32_t pk = 0;                  // promotion partials issued (buffer = pk & 1)
             // Promotion tiles: the epilogue reads each K block's scales from the
             // scale ring, so an entry is released (sfempty) only once the epilogue
-            // has read every partial of its stage.  The MMA warp learns that from
+            // has read every partial of its stage.  The MMA thread learns that from
             // its own tempty waits (the wait for partial p passes once partial p-2
             // has been read); entries wait here, oldest first, with the index of
             // their last partial.
             int pend_f0 = -1, pend_l0 = 0, pend_f1 = -1, pend_l1 = 0;
             // A pair's peer: in promotion tiles its epilogue releases a partial on
-            // its own barrier only, and this warp, which waits there anyway,
+            // its own barrier only, and this thread, which waits there anyway,
             // forwards the release to the leader as one arrival counting for the
             // peer's eight warps (bit b: buffer b's last use still to forward).
             uint32_t fwd = 0;
