@@ -13,9 +13,11 @@ per step exceed the L2, so it runs without the flush, and its read-flushed and
 write-flushed times are reported beside it), the 8192^3 arbitrary-scale GEMM
 with outliers (promotion path; also with the path pinned), the block
 quantization of 8192x8192 bf16 activations (GB/s against HBM), the 4096^3 GEMM
-with per-token x per-channel scales and the 4096^3 GEMM with a fused residual
-add.  Every generated input buffer is recorded by its SHA-256, with the torch
-version that generated it.
+with per-token x per-channel scales, the 4096^3 GEMM with a fused residual
+add, the per-token-scale 4096^3 GEMMs, and the prefill GEMM with its output
+quantized to E4M3 in the epilogue (beside the same work unfused: the bf16 GEMM
+followed by the block quantizer).  Every generated input buffer is recorded by
+its SHA-256, with the torch version that generated it.
 
 ``--impl reference`` times the CPU oracle (the only other implementation of
 the method; plain C, fp64) on a bounded sample of the same workload.
@@ -56,6 +58,8 @@ WORKLOAD_NAMES = {
     "q8": "block quantization of bf16 activations 8192x8192 -> E4M3 codes + 32x32 fp32 scales",
     "r1": "per-token x per-channel scaled E4M3 GEMM M=N=K=4096 (fp32 scales [M] and [N]), bf16 out",
     "f1": "block-scaled E4M3 GEMM M=N=K=4096 with a bf16 residual added in the epilogue",
+    "qo": ("block-scaled E4M3 GEMM M=8192, N=28672, K=8192 (pow2 32x32 scales) whose output is quantized "
+           "in the epilogue to E4M3 codes + 32x32 fp32 scales"),
     "p1": "per-token A scales (one fp32 per row per 32-K block) x 32x32 B blocks, E4M3 GEMM M=N=K=4096, bf16 out",
     "p1n": "per-token power-of-two A scales (one per row per 32-K block, UE8M0 on the MMA) x 32x32 pow2 B blocks, "
            "E4M3 GEMM M=N=K=4096 (mode NATIVE), bf16 out",
@@ -219,6 +223,23 @@ def make_runner(name, dev, bs):
         def run(stream):
             bs.fp8_quantize_blocks(x, q, sc, stream=stream)
         return run, 0, nbytes, {"x": x}
+    if name in ("qo", "qo_chain"):
+        # the prefill GEMM with its output quantized for the next layer: fused in the
+        # epilogue (qo), or the bf16 GEMM followed by the block quantizer (qo_chain)
+        p = workloads.make("c2", seed=0, device=dev)
+        Cq = torch.empty(p.M, p.N, dtype=torch.uint8, device=dev)
+        sC = torch.empty(p.M // 32, p.N // 32, dtype=torch.float32, device=dev)
+        nbytes = p.M * p.K + p.N * p.K + 4 * (p.sA.numel() + p.sB.numel()) + p.M * p.N + 4 * sC.numel()
+        if name == "qo":
+            def run(stream):
+                bs.fp8_gemm_blockscaled_quant(p.A, p.sA, p.B, p.sB, Cq, sC, p.M, p.N, p.K, stream=stream)
+        else:
+            C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
+
+            def run(stream):
+                bs.fp8_gemm_blockscaled(p.A, p.sA, p.B, p.sB, C, p.M, p.N, p.K, stream=stream)
+                bs.fp8_quantize_blocks(C, Cq, sC, stream=stream)
+        return run, p.flops, nbytes, {"A": p.A, "sA": p.sA, "B": p.B, "sB": p.sB}
     if name == "f1":
         p = workloads.make("c1", seed=0, device=dev)
         g = torch.Generator(device=dev).manual_seed(1)
@@ -605,7 +626,7 @@ def run_ours(args):
 
     results = {}
     hashes = {}
-    names = [HEADLINE] + ([] if args.headline_only else ["c1", "c3", "c4", "c4p", "q8", "r1", "f1", "p1", "p1n"])
+    names = [HEADLINE] + ([] if args.headline_only else ["c1", "c3", "c4", "c4p", "q8", "r1", "f1", "p1", "p1n", "qo"])
     if args.only:
         names = [args.only]
     launches = 0
@@ -620,6 +641,13 @@ def run_ours(args):
             mean_ms = max_over_ranks(sum(ms) / len(ms), world)
             results[name] = {"ms": mean_ms, "flops": flops, "bytes": nbytes,
                              "ms_min": min(ms), "ms_median": statistics.median(ms)}
+            if name == "qo" and not args.only:
+                # the same work unfused: bf16 GEMM, then the block quantizer (two launches)
+                run_c, _, _, _ = make_runner("qo_chain", dev, bs)
+                msc = time_device(run_c, args.steps, args.warmup, dev, flush, world, flush="write")
+                launches += 2 * args.steps
+                results[name]["ms_chain"] = max_over_ranks(sum(msc) / len(msc), world)
+                del run_c
             if name in EXTRA_FLUSH and not args.only:
                 for how in EXTRA_FLUSH[name]:
                     msf = time_device(run, args.steps, args.warmup, dev, flush, world, flush=how)
@@ -692,6 +720,11 @@ def run_ours(args):
         else:
             entry["value"] = round(r["flops"] / (r["ms"] * 1e-3) / 1e12, 1)
             entry["unit"] = "TFLOP/s"
+            if "ms_chain" in r:
+                entry["unfused_chain"] = {"ms_per_step": round(r["ms_chain"], 4),
+                                          "value": round(r["flops"] / (r["ms_chain"] * 1e-3) / 1e12, 1),
+                                          "unit": "TFLOP/s",
+                                          "how": "fp8_gemm_blockscaled (bf16 out) then fp8_quantize_blocks"}
         extra[name] = entry
 
     line = {
@@ -789,7 +822,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-elements", type=int, default=65536)
-    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "c4p", "q8", "r1", "f1", "p1", "p1n"], default=None,
+    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "c4p", "q8", "r1", "f1", "p1", "p1n", "qo"], default=None,
                     help="time one workload only (no e2e, no CPU baseline): profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:

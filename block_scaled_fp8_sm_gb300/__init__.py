@@ -18,7 +18,7 @@ from ._abi import (FP8_PATH_AUTO, FP8_PATH_NATIVE, FP8_PATH_PROMOTE,  # noqa: F4
 __all__ = ["fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_gemm_grouped", "group_descs",
            "fp8_gemm_grouped_device", "fp8_grouped_workspace_bytes", "group_table", "fp8_gemm_pertoken",
            "fp8_quantize_blocks", "fp8_gemm_rowcol", "fp8_gemm_blockscaled_residual",
-           "fp8_status_query", "fp8_strerror", "fp8_version", "fp8_debug_set", "fp8_lib_shutdown",
+           "fp8_gemm_blockscaled_quant", "fp8_status_query", "fp8_strerror", "fp8_version", "fp8_debug_set", "fp8_lib_shutdown",
            "Fp8Error", "library"]
 
 
@@ -92,6 +92,19 @@ def fp8_gemm_blockscaled_residual(A, sA, B, sB, R, C, M=None, N=None, K=None, st
     _check(library().fp8_gemm_blockscaled_residual(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(R), _ptr(C),
                                                    M, N, K, _stream(stream)), "fp8_gemm_blockscaled_residual")
     return C
+
+
+def fp8_gemm_blockscaled_quant(A, sA, B, sB, Cq, sC, M=None, N=None, K=None, stream=None):
+    """(Cq, sC) = block quantization of the block-scaled GEMM's bf16 output, done
+    in its epilogue: Cq E4M3 codes [M, N] (uint8 or float8 storage), sC fp32
+    [ceil(M/32), N/32] scales; equal bit for bit to fp8_gemm_blockscaled
+    followed by fp8_quantize_blocks."""
+    M = A.shape[0] if M is None else M
+    K = A.shape[1] if K is None else K
+    N = B.shape[0] if N is None else N
+    _check(library().fp8_gemm_blockscaled_quant(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(Cq), _ptr(sC),
+                                                M, N, K, _stream(stream)), "fp8_gemm_blockscaled_quant")
+    return Cq, sC
 
 
 def fp8_gemm_rowcol(A, sA, B, sB, C, M=None, N=None, K=None, stream=None):

@@ -74,6 +74,9 @@ int set_kernel_attrs() {
     if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN, SCALE_BLOCK32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN, true>()) != cudaSuccess)
         return FP8_ERR_CUDA;
+    if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN, SCALE_BLOCK32, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BN, true>()) != cudaSuccess)
+        return FP8_ERR_CUDA;
     static_assert(smem_bytes<BN, true, false, true>() <= 232448, "shared memory of the per-token pair kernel");
     if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN, SCALE_TOKEN, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN, true, false, true>()) != cudaSuccess)
@@ -174,11 +177,24 @@ int encode_out_raw(CUtensorMap *m, void *C, int64_t M, int64_t N) {
     return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
 }
 
+// E4M3 output codes (M x N bytes, row-major) for the quantized-output
+// epilogue: box of 32 bytes x BM rows, no swizzle; rows past M are clipped.
+int encode_outq_raw(CUtensorMap *m, void *Cq, int64_t M, int64_t N) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
+    const cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(BM)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, Cq, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
 // A tensor map is a pure function of its encode arguments, so one cached by
 // those arguments stays valid whatever later happens to the memory behind it.
 // The cache saves the host ~2 us per map (a grouped call encodes one per group).
 struct MapKey {
-    int kind;   // 0: 2D K-major, 1: 3D K-major halves, 2: bf16 output
+    int kind;   // 0: 2D K-major, 1: 3D K-major halves, 2: bf16 output, 3: E4M3 output
     int box;
     const void *base;
     int64_t a, b;
@@ -227,6 +243,9 @@ int encode_kmajor_halves(CUtensorMap *m, const void *base, int64_t rows, int64_t
 }
 int encode_out(CUtensorMap *m, void *C, int64_t M, int64_t N) {
     return cached_map(m, MapKey{2, BM, C, M, N}, [&](CUtensorMap *o) { return encode_out_raw(o, C, M, N); });
+}
+int encode_outq(CUtensorMap *m, void *Cq, int64_t M, int64_t N) {
+    return cached_map(m, MapKey{3, BM, Cq, M, N}, [&](CUtensorMap *o) { return encode_outq_raw(o, Cq, M, N); });
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -303,10 +322,10 @@ int launch_plain(const void *A, const float *sA, const void *B, const float *sB,
 
 // CTA-pair launch: 256-row tiles, each CTA of a pair loads 128 rows of A and
 // 128 of B's 256 columns; the grid is a whole number of pairs.
-template <int BN, int SK = SCALE_BLOCK32, bool RES = false>
+template <int BN, int SK = SCALE_BLOCK32, bool RES = false, bool QOUT = false>
 int launch_pair(const void *A, const float *sA, const void *B, const float *sB, void *C,
                 int64_t M, int64_t N, int64_t K, int mode, DeviceState *d, cudaStream_t stream,
-                const void *R = nullptr) {
+                const void *R = nullptr, float *sC = nullptr) {
     PlainArgs args;
     std::memset(&args, 0, sizeof args);
     fill_common(args.c, M, N, K, mode, d, BN);
@@ -316,7 +335,13 @@ int launch_pair(const void *A, const float *sA, const void *B, const float *sB, 
     if (rc != FP8_OK) return rc;
     rc = encode_kmajor(&args.tmB, B, N, K, BN / 2);
     if (rc != FP8_OK) return rc;
-    rc = encode_out(&args.tmC, C, M, N);
+    if constexpr (QOUT) {   // C holds the E4M3 codes
+        rc = encode_outq(&args.tmQ, C, M, N);
+        args.Cq = static_cast<uint8_t *>(C);
+        args.sC = sC;
+    } else {
+        rc = encode_out(&args.tmC, C, M, N);
+    }
     if (rc != FP8_OK) return rc;
     rc = encode_kmajor_halves(&args.tmA3, A, M, K, BM);
     if (rc != FP8_OK) return rc;
@@ -332,8 +357,8 @@ int launch_pair(const void *A, const float *sA, const void *B, const float *sB, 
         if (rc != FP8_OK) return rc;
     }
     const int pairs = args.c.num_tiles < d->sm_count / 2 ? args.c.num_tiles : d->sm_count / 2;
-    bsfp8_gemm_pair<BN, SK, RES><<<2 * pairs, NUM_THREADS, smem_bytes<BN, true, false, SK == SCALE_TOKEN>(), stream>>>(
-        args);
+    bsfp8_gemm_pair<BN, SK, RES, QOUT>
+        <<<2 * pairs, NUM_THREADS, smem_bytes<BN, true, false, SK == SCALE_TOKEN>(), stream>>>(args);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -572,6 +597,34 @@ int fp8_gemm_blockscaled_residual(const void *A, const float *sA, const void *B,
                    : FP8_ERR_CUDA;
     }
     return launch_pair<TILE_N, SCALE_BLOCK32, true>(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, d, stream, R);
+}
+
+int fp8_gemm_blockscaled_quant(const void *A, const float *sA, const void *B, const float *sB, void *Cq,
+                               float *sC, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != FP8_OK) return rc;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!Cq || !sC) return FP8_ERR_NULL;
+    if (!aligned(Cq, 16) || !aligned(sC, 4)) return FP8_ERR_ALIGN;
+    if (K > 0) {
+        if (!A || !B || !sA || !sB) return FP8_ERR_NULL;
+        if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 4) || !aligned(sB, 4))
+            return FP8_ERR_ALIGN;
+    }
+    DeviceState *d = nullptr;
+    rc = device_setup(&d);
+    if (rc != FP8_OK) return rc;
+    if (K == 0) {   // C = 0: every block all zero, so codes 0 and scales 1
+        rc = zero_fill(Cq, M * N / 2, stream);
+        if (rc != FP8_OK) return rc;
+        const int64_t ns = (M + 31) / 32 * (N / 32);
+        int blocks = static_cast<int>(ns / 256 + 1);
+        if (blocks > 4096) blocks = 4096;
+        bsfp8_fill_f32<<<blocks, 256, 0, stream>>>(sC, 1.0f, ns);
+        return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+    }
+    return launch_pair<TILE_N, SCALE_BLOCK32, false, true>(A, sA, B, sB, Cq, M, N, K, FP8_PATH_AUTO, d, stream,
+                                                           nullptr, sC);
 }
 
 int fp8_gemm_rowcol(const void *A, const float *sA, const void *B, const float *sB, void *C,

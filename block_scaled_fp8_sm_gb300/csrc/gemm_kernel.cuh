@@ -76,6 +76,7 @@
 #include <type_traits>
 
 #include "ptx.cuh"
+#include "quant_kernel.cuh"
 
 namespace bsfp8 {
 
@@ -212,6 +213,9 @@ struct PlainArgs {
     Common c;
     CUtensorMap tmR;    // residual kernels: bf16 residual, same shape and box as C
     const __nv_bfloat16 *R;
+    CUtensorMap tmQ;    // quantized-output kernels: E4M3 codes {N, M} bytes, box {32, 128}
+    uint8_t *Cq;        //   the codes [M][N] and the block scales [ceil(M/32)][N/32]
+    float *sC;
 };
 
 struct GroupedArgs {
@@ -505,6 +509,23 @@ __device__ __forceinline__ void store_bf16x32f(__nv_bfloat16 *dst, const float *
     }
 }
 
+// 32 fp32 values (bits or floats) -> 16 words of bf16 pairs (nearest even), or
+// zeros for a row that does not exist.
+__device__ __forceinline__ void bf16_words32(uint32_t (&o)[16], const uint32_t *r, bool keep) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+        o[j] = keep ? *reinterpret_cast<uint32_t *>(&pr) : 0u;
+    }
+}
+__device__ __forceinline__ void bf16_words32f(uint32_t (&o)[16], const float *v, bool keep) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+        o[j] = keep ? *reinterpret_cast<uint32_t *>(&pr) : 0u;
+    }
+}
+
 // One-CTA / CTA-pair forms of the tensor-core issue steps.
 template <bool PAIR>
 __device__ __forceinline__ void cp_lines(uint32_t taddr, uint64_t sdesc) {
@@ -557,9 +578,13 @@ __device__ __forceinline__ void issue_native_stage(uint32_t tmem, uint32_t sfa, 
 }
 
 // ---------------------------------------------------------------------------
-// SK: scale layout; RES: a bf16 residual is added before the bf16 rounding.
-template <int BN, bool GROUPED, bool PAIR, typename Args, int SK = SCALE_BLOCK32, bool RES = false>
+// SK: scale layout; RES: a bf16 residual is added before the bf16 rounding;
+// QOUT: the bf16 output is quantized to E4M3 codes with one scale per 32 x 32
+// block (the block quantizer's arithmetic) instead of being stored.
+template <int BN, bool GROUPED, bool PAIR, typename Args, int SK = SCALE_BLOCK32, bool RES = false,
+          bool QOUT = false>
 __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
+    static_assert(!QOUT || (PAIR && !RES && SK == SCALE_BLOCK32), "quantized output: block-scaled pair kernel");
     // per-token scales run the native path on CTA pairs (per-row scale lines)
     // and the promotion path on single CTAs
     using C = Cfg<BN, PAIR, GROUPED, PAIR && SK == SCALE_TOKEN>;
@@ -1406,13 +1431,30 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                                 add_bf16x32(r[x], mine);
                             }
                         }
-                        pack_bf16x32(mine, r[x]);
+                        if constexpr (QOUT) {
+                            // the warp's 32 rows x these 32 columns are one 32 x 32 block:
+                            // bf16, block scale, codes; the codes go out by TMA as a
+                            // 128 x 32-byte box, the scale by lane 0
+                            uint32_t bw[16], cd[8];
+                            bf16_words32(bw, r[x], row_ok);
+                            const float sc = quantize_rows32(bw, cd);
+                            uint4 *qm = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(stg) + (32 * q + lane) * 32);
+                            qm[0] = make_uint4(cd[0], cd[1], cd[2], cd[3]);
+                            qm[1] = make_uint4(cd[4], cd[5], cd[6], cd[7]);
+                            const int col = tt.n0 + col0 + 32 * x;
+                            const int rb0 = tt.m0 + row_off + 32 * q;   // the block's first row
+                            if (lane == 0 && col < c.N && rb0 < c.M)
+                                args.sC[static_cast<int64_t>(rb0 / 32) * (c.N / 32) + col / 32] = sc;
+                        } else {
+                            pack_bf16x32(mine, r[x]);
+                        }
                         fence_proxy_async_smem();
                         named_bar_sync(bar_id, HALF_THREADS);
                         if (issuer) {
                             const int col = tt.n0 + col0 + 32 * x;
                             if (col < c.N) {
-                                tma_store_2d(&args.tmC, stg, col, tt.m0 + row_off);
+                                if constexpr (QOUT) tma_store_2d(&args.tmQ, stg, col, tt.m0 + row_off);
+                                else tma_store_2d(&args.tmC, stg, col, tt.m0 + row_off);
                                 bulk_commit_group();
                                 bulk_wait_read_all();
                             }
@@ -1500,7 +1542,27 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                 }
                 if constexpr (TMA_OUT) ok = named_bar_and(bar_id, HALF_THREADS, ok);
                 if (!ok) break;
-                if (row_ok) {
+                if constexpr (QOUT) {
+                    // every lane takes part in each block's maximum; codes and
+                    // scales go out by plain stores
+#pragma unroll
+                    for (int x = 0; x < NCH; ++x) {
+                        uint32_t bw[16], cd[8];
+                        bf16_words32f(bw, acc + 32 * x, row_ok);
+                        const float sc = quantize_rows32(bw, cd);
+                        const int col = tt.n0 + col0 + 32 * x;
+                        const int rb0 = tt.m0 + row_off + 32 * q;
+                        if (col < c.N) {
+                            if (row_ok) {
+                                uint4 *dq = reinterpret_cast<uint4 *>(args.Cq + static_cast<int64_t>(row) * c.N + col);
+                                dq[0] = make_uint4(cd[0], cd[1], cd[2], cd[3]);
+                                dq[1] = make_uint4(cd[4], cd[5], cd[6], cd[7]);
+                            }
+                            if (lane == 0 && rb0 < c.M)
+                                args.sC[static_cast<int64_t>(rb0 / 32) * (c.N / 32) + col / 32] = sc;
+                        }
+                    }
+                } else if (row_ok) {
 #pragma unroll
                     for (int x = 0; x < NCH; ++x) {
                         if (tt.n0 + col0 + 32 * x >= c.N) continue;
@@ -1553,11 +1615,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bsfp8_gemm_plain(const __grid_
 }
 
 // CTA-pair variant: clusters of two CTAs, 256-row tiles, pair MMAs.
-template <int BN, int SK = SCALE_BLOCK32, bool RES = false>
+template <int BN, int SK = SCALE_BLOCK32, bool RES = false, bool QOUT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     bsfp8_gemm_pair(const __grid_constant__ PlainArgs args) {
     extern __shared__ uint8_t smem_raw[];
-    gemm_body<BN, false, true, PlainArgs, SK, RES>(args, smem_raw);
+    gemm_body<BN, false, true, PlainArgs, SK, RES, QOUT>(args, smem_raw);
 }
 
 template <int BN>
@@ -1606,6 +1668,12 @@ __global__ void bsfp8_zero_fill(uint4 *p, int64_t n16) {
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
         p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+__global__ void bsfp8_fill_f32(float *p, float v, int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        p[i] = v;
 }
 
 }  // namespace bsfp8

@@ -94,6 +94,32 @@ __device__ __forceinline__ uint2 codes8(const uint32_t (&w)[4], float s, float n
                       __byte_perm(e4m3x2(v[4], v[5]), e4m3x2(v[6], v[7]), 0x5410) ^ 0x80808080u);
 }
 
+// One 32 x 32 block held by a warp, one row per lane: the lane's 32 bf16 values
+// in bf[16] (columns 2j and 2j+1 in word j).  Returns the block's scale (its
+// maximum over all 32 lanes) and leaves the lane's 32 codes in codes[8] (byte b
+// of word w: column 4w + b) -- the quantizer's arithmetic above, so the codes
+// and scale equal those of fp8_quantize_blocks on the same bf16 values.  Every
+// lane of the warp must call it (shuffles); rows that do not exist pass zeros.
+__device__ __forceinline__ float quantize_rows32(const uint32_t (&bf)[16], uint32_t (&codes)[8]) {
+    uint32_t am2 = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) am2 = absmax_bf16x2(am2, bf[j]);
+    float amax = fmaxf(__uint_as_float(am2 << 16), __uint_as_float(am2 & 0xFFFF0000u));
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float sc = block_scale(amax);
+    const bool recip = sc >= 0x1p-100f && sc <= 3.40282347e38f;   // the same for the whole warp
+    const float nrc = recip ? -__frcp_rn(sc) : 0.0f;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint32_t w[4] = {bf[4 * g], bf[4 * g + 1], bf[4 * g + 2], bf[4 * g + 3]};
+        const uint2 cc = recip ? codes8<true>(w, sc, nrc) : codes8<false>(w, sc, 0.0f);
+        codes[2 * g] = cc.x;
+        codes[2 * g + 1] = cc.y;
+    }
+    return sc;
+}
+
 // Codes of the lane's four rows of the strip (the path is chosen once per strip).
 template <bool RECIP>
 __device__ __forceinline__ void store_codes(const uint32_t (&w)[4][4], float s, float nrc, uint8_t *q, int64_t r0,

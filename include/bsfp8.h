@@ -116,6 +116,24 @@ int fp8_gemm_blockscaled_residual(const void *A, const float *sA, const void *B,
                                   const void *R, void *C, int64_t M, int64_t N, int64_t K,
                                   cudaStream_t stream);
 
+/* Block-scaled GEMM whose output is quantized in the epilogue to the operand
+ * format of the next GEMM (FP8 GEMM library article, hncyxsy.com/news/241433,
+ * sections 2.1-2.2: E4M3 with one fp32 scale per 32x32 block; section 2.3:
+ * element-wise work fused into the GEMM's tail instead of another pass over
+ * the output):
+ *   (Cq, sC) = fp8_quantize_blocks( fp8_gemm_blockscaled(A, sA, B, sB) )
+ * bit for bit: the bf16 output of the AUTO-path GEMM is never written; each
+ * 32x32 block of it gets s = amax/448 (1 for an all-zero block) and codes
+ * E4M3(x/s) with the quantizer's arithmetic.  A 32-row block's scale depends
+ * on all its rows, so results are batch-invariant per 32-row block.
+ * Cq: E4M3 codes [M, N] row-major (16-byte aligned), fully overwritten.
+ * sC: fp32 [ceil(M/32), N/32] row-major (4-byte aligned), fully overwritten.
+ * Everything else as fp8_gemm_blockscaled; K = 0 gives codes 0 and scales 1.
+ * Returns FP8_OK or FP8_ERR_SHAPE / FP8_ERR_NULL / FP8_ERR_ALIGN / FP8_ERR_CUDA. */
+int fp8_gemm_blockscaled_quant(const void *A, const float *sA, const void *B, const float *sB,
+                               void *Cq, float *sC, int64_t M, int64_t N, int64_t K,
+                               cudaStream_t stream);
+
 /* GEMM with scales that do not vary along K (FP8 GEMM library article,
  * hncyxsy.com/news/241433, section 2.2: per-tensor, per-channel and per-token
  * scale granularities; section 2.3: such scales are applied in the GEMM's

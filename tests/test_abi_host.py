@@ -70,6 +70,24 @@ def test_pertoken_argument_errors(lib):
     assert call(A=0, sA=0, B=0, sB=0, C=0, M=0, mode=_abi.FP8_PATH_NATIVE) == _abi.FP8_OK
 
 
+def test_quant_out_argument_errors(lib):
+    def call(**kw):
+        a = dict(A=16, sA=16, B=16, sB=16, Cq=16, sC=16, M=64, N=64, K=64)
+        a.update(kw)
+        return lib.fp8_gemm_blockscaled_quant(a["A"], a["sA"], a["B"], a["sB"], a["Cq"], a["sC"],
+                                              a["M"], a["N"], a["K"], None)
+    assert call(N=33) == _abi.FP8_ERR_SHAPE
+    assert call(K=48) == _abi.FP8_ERR_SHAPE
+    assert call(M=-1) == _abi.FP8_ERR_SHAPE
+    assert call(Cq=0) == _abi.FP8_ERR_NULL
+    assert call(sC=0) == _abi.FP8_ERR_NULL
+    assert call(A=0) == _abi.FP8_ERR_NULL
+    assert call(Cq=8) == _abi.FP8_ERR_ALIGN
+    assert call(sC=2) == _abi.FP8_ERR_ALIGN
+    assert call(B=24) == _abi.FP8_ERR_ALIGN
+    assert call(A=0, sA=0, B=0, sB=0, Cq=0, sC=0, M=0) == _abi.FP8_OK
+
+
 def test_empty_problems_enqueue_nothing(lib):
     # M == 0 or N == 0: OK without any device work (no device needed)
     assert _call(lib, A=0, sA=0, B=0, sB=0, C=0, M=0) == _abi.FP8_OK
