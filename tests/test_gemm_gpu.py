@@ -78,6 +78,16 @@ def test_ragged_native(bs, M, N, K):
     _full_check(bs, _rand_problem(M, N, K, seed=M + N + K))
 
 
+@pytest.mark.parametrize("pow2", [True, False])
+def test_multi_tile_partial_last_stage(bs, pow2):
+    """4096 x 2560 x 1056: 160 pair tiles on 76 pairs (every pair runs two or
+    three tiles) whose K loop ends in a partial 256-K stage (1056 = 4 x 256 +
+    32): the full-stage straight line and the guarded stage body alternate
+    within each tile, on both paths.  Compared in full."""
+    _full_check(bs, _rand_problem(4096, 2560, 1056, seed=77 + pow2, pow2=pow2))
+    assert bs.fp8_status_query() == 0
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 32, 32), (45, 96, 160), (130, 288, 480), (256, 256, 1024)])
 def test_ragged_promote_arbitrary_scales(bs, M, N, K):
     _full_check(bs, _rand_problem(M, N, K, seed=M * 3 + K, pow2=False))
