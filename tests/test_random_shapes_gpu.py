@@ -2,10 +2,11 @@
 C ABI, against the oracle: M from 1 to 300, N and K multiples of 32 from 32 to
 512 (one-block N and K, K ending inside a 128-K stage, M ending inside a
 32-row block, tiles cut at every edge).  Per shape: the block-scaled call in
-each path mode, the allocation-free call, the residual, per-token x
-per-channel and per-token calls, and a two-group grouped launch; the
-allocation-free call and the pinned promotion path are also compared with the
-regular call bit for bit where their contracts say they agree."""
+each path mode, the allocation-free call, the quantized-output call, the
+residual, per-token x per-channel and per-token calls, and a two-group grouped
+launch; the allocation-free call, the pinned promotion path and the
+quantized-output call are also compared with the regular call (followed by
+the block quantizer) bit for bit where their contracts say they agree."""
 import numpy as np
 import pytest
 import torch
@@ -74,6 +75,18 @@ def test_random_shape_every_entry_point(bs, i):
         torch.cuda.synchronize()
         assert bs.fp8_status_query() == 0
         assert torch.equal(C.view(torch.int16), res[None].view(torch.int16))
+
+    # output quantized in the epilogue: the bf16 call followed by the quantizer, bit for bit
+    for sA, sB in ((sA_p, sB_p), (sA_a, sB_a)):
+        C = out()
+        bs.fp8_gemm_blockscaled(dA, sA.to(DEV), dB, sB.to(DEV), C, M, N, K)
+        q_ref, s_ref = bs.fp8_quantize_blocks(C)
+        Cq = torch.empty(M, N, dtype=torch.uint8, device=DEV)
+        sC = torch.empty((M + 31) // 32, N // 32, dtype=torch.float32, device=DEV)
+        bs.fp8_gemm_blockscaled_quant(dA, sA.to(DEV), dB, sB.to(DEV), Cq, sC, M, N, K)
+        torch.cuda.synchronize()
+        assert bs.fp8_status_query() == 0
+        assert torch.equal(Cq, q_ref) and torch.equal(sC.view(torch.int32), s_ref.view(torch.int32)), f"{tag} quant"
 
     # residual (in place)
     gr = torch.Generator().manual_seed(3000 + i)
