@@ -1371,7 +1371,11 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
             }
 
             if (!promote) {
-                ok = __all_sync(FULL, wait_poll(&ctl->tfull[0], uses0 & 1u, ctl, c));
+                // One warp per column half polls for the accumulator: the one of lane
+                // quarter 0, whose sub-partition the MMA thread does not share; the
+                // half's other warps wait in its named barrier.  Polling warps beside
+                // the MMA thread slow its issue (4-6 % on the prefill GEMM).
+                if (!TMA_OUT || q == 0) ok = __all_sync(FULL, wait_poll(&ctl->tfull[0], uses0 & 1u, ctl, c));
                 if constexpr (TMA_OUT) ok = named_bar_and(bar_id, HALF_THREADS, ok);
                 if (!ok) break;
                 if (warp == EPI_WARP0 && lane == 0) trace_event(c, TR_EPI_FULL, i);
