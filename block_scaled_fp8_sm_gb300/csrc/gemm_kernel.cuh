@@ -550,9 +550,15 @@ __device__ __forceinline__ void commit_to(uint64_t *bar) {
 // issued as one straight line: the tensor pipe holds about one MMA, so a
 // branch between two MMAs delays the second one's issue past the first one's
 // end (a full stage measured ~5 % faster on the prefill GEMM without them).
+// Wide full stages also test the next stage's two barriers (nb0/np0,
+// nb1/np1) inside the asm block of their last two MMAs and return the result
+// (3.5-4.8 % on the prefill GEMM against a test after the commits); other
+// stages return 0 and the caller tests after them.
 template <typename C, bool FULL>
-__device__ __forceinline__ void issue_native_stage(uint32_t tmem, uint32_t sfa, uint32_t sf_s, uint64_t ad,
-                                                   uint64_t bd, int nk, uint32_t acc0) {
+__device__ __forceinline__ uint32_t issue_native_stage(uint32_t tmem, uint32_t sfa, uint32_t sf_s, uint64_t ad,
+                                                       uint64_t bd, int nk, uint32_t acc0, uint64_t *nb0,
+                                                       uint32_t np0, uint64_t *nb1, uint32_t np1) {
+    constexpr bool TAIL_TEST = FULL && C::HALVES == 2;
 #pragma unroll
     for (int hh = 0; hh < C::HALVES; ++hh) {
         if (FULL || hh * KB_PER_STAGE < nk) {
@@ -568,12 +574,23 @@ __device__ __forceinline__ void issue_native_stage(uint32_t tmem, uint32_t sfa, 
     for (int hh = 0; hh < C::HALVES; ++hh) {
 #pragma unroll
         for (int j = 0; j < KB_PER_STAGE; ++j) {
+            if (TAIL_TEST && hh == 1 && j >= KB_PER_STAGE - 2) continue;   // issued with the test below
             if (FULL || hh * KB_PER_STAGE + j < nk)
                 mma_block<C::PAIR>(tmem, ad + static_cast<uint64_t>((hh * C::A_HALF >> 4) + 2 * j),
                                    bd + static_cast<uint64_t>((hh * C::B_HALF >> 4) + 2 * j),
                                    idesc_mxf8f6f4(C::MMA_M, C::BN, j, j), sfa + hh * C::SF_COLS,
                                    sfa + hh * C::SF_COLS + 4, (hh | j) != 0 ? 1u : acc0);
         }
+    }
+    if constexpr (TAIL_TEST) {
+        constexpr int j0 = KB_PER_STAGE - 2, j1 = KB_PER_STAGE - 1;
+        return mma_mxf8_x2_test<C::PAIR>(
+            tmem, ad + static_cast<uint64_t>((C::A_HALF >> 4) + 2 * j0), bd + static_cast<uint64_t>((C::B_HALF >> 4) + 2 * j0),
+            idesc_mxf8f6f4(C::MMA_M, C::BN, j0, j0), ad + static_cast<uint64_t>((C::A_HALF >> 4) + 2 * j1),
+            bd + static_cast<uint64_t>((C::B_HALF >> 4) + 2 * j1), idesc_mxf8f6f4(C::MMA_M, C::BN, j1, j1),
+            sfa + C::SF_COLS, sfa + C::SF_COLS + 4, nb0, np0, nb1, np1);
+    } else {
+        return 0u;
     }
 }
 
@@ -890,10 +907,11 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                         uint32_t ph = static_cast<uint32_t>(ot / S) & 1u, phf = static_cast<uint32_t>(ot / FS) & 1u;
                         trace_event(c, TR_MMA_LOOP, i);
                         // One operand stage: its barriers (unless the previous stage found
-                        // them complete), scale copies and MMAs, commits; then the next
-                        // stage's barriers are tested (without blocking, one test of both,
-                        // no branch) while the last MMA still runs.  Each branch of this
-                        // single thread costs tens of cycles in which the pipe may run dry.
+                        // them complete), scale copies and MMAs, commits; the next stage's
+                        // barriers are tested without blocking (one test of both, with the
+                        // last two MMAs on wide stages, else after the commits).  Each
+                        // branch of this single thread costs tens of cycles in which the
+                        // pipe may run dry.
                         bool next_ready = false;
                         auto stage = [&](auto full, int w) -> bool {
                             if (!next_ready &&
@@ -907,14 +925,18 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                             const uint64_t bd = sdesc_k_sw128(smem_u32(sm_b + s * C::B_BYTES));
                             const int nk = decltype(full)::value ? C::HALVES * KB_PER_STAGE
                                                                  : min(C::HALVES * KB_PER_STAGE, c.KB - w * C::HALVES * KB_PER_STAGE);
-                            issue_native_stage<C, decltype(full)::value>(tmem, sfa, sf_s, ad, bd, nk, w != 0 ? 1u : 0u);
+                            const int s2 = s + 1 == S ? 0 : s + 1, f2 = f + 1 == FS ? 0 : f + 1;
+                            const uint32_t ph2 = ph ^ (s2 == 0 ? 1u : 0u), phf2 = phf ^ (f2 == 0 ? 1u : 0u);
+                            uint32_t t = issue_native_stage<C, decltype(full)::value>(
+                                tmem, sfa, sf_s, ad, bd, nk, w != 0 ? 1u : 0u, &ctl->sfready[f2], phf2, &ctl->full[s2], ph2);
                             commit_to<PAIR>(&ctl->empty[s]);
                             commit_to<PAIR>(&ctl->sfempty[f]);
-                            s = s + 1 == S ? 0 : s + 1;
-                            ph ^= s == 0 ? 1u : 0u;
-                            f = f + 1 == FS ? 0 : f + 1;
-                            phf ^= f == 0 ? 1u : 0u;
-                            next_ready = mbar_test_wait2(&ctl->sfready[f], phf, &ctl->full[s], ph) & (w + 1 < KW);
+                            s = s2;
+                            f = f2;
+                            ph = ph2;
+                            phf = phf2;
+                            if (!(decltype(full)::value && C::HALVES == 2)) t = mbar_test_wait2(&ctl->sfready[f], phf, &ctl->full[s], ph);
+                            next_ready = (t != 0u) & (w + 1 < KW);
                             return true;
                         };
                         // Full stages first, as straight lines of copies and MMAs; a

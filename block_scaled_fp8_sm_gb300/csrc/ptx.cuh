@@ -92,6 +92,48 @@ __device__ __forceinline__ bool mbar_test_wait2(uint64_t *b0, uint32_t p0, uint6
     return ok != 0u;
 }
 
+// The last two block-scaled MMAs of an operand stage (both accumulating) and,
+// in the same asm block, a non-blocking test of two barrier phases whose result
+// is consumed only after both MMAs are issued: the test's shared-memory latency
+// then overlaps the MMAs instead of stalling the issuing thread between stages.
+// Returns whether both phases have completed.
+template <bool PAIR>
+__device__ __forceinline__ uint32_t mma_mxf8_x2_test(uint32_t d, uint64_t a0, uint64_t b0, uint32_t i0,
+                                                     uint64_t a1, uint64_t b1, uint32_t i1, uint32_t sfa,
+                                                     uint32_t sfb, uint64_t *bar0, uint32_t p0, uint64_t *bar1,
+                                                     uint32_t p1) {
+    uint32_t ok;
+    if constexpr (PAIR)
+        asm volatile(
+            "{\n\t.reg .pred p, q, t;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+            "setp.eq.u32 t, 0, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], %6, %7, %8, [%9], [%10], t;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], %11, %12, %13, [%9], [%10], t;\n\t"
+            "and.pred p, p, q;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar0)), "r"(p0), "r"(smem_u32(bar1)), "r"(p1), "r"(d), "l"(a0), "l"(b0), "r"(i0),
+              "r"(sfa), "r"(sfb), "l"(a1), "l"(b1), "r"(i1)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p, q, t;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+            "setp.eq.u32 t, 0, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], %6, %7, %8, [%9], [%10], t;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%5], %11, %12, %13, [%9], [%10], t;\n\t"
+            "and.pred p, p, q;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar0)), "r"(p0), "r"(smem_u32(bar1)), "r"(p1), "r"(d), "l"(a0), "l"(b0), "r"(i0),
+              "r"(sfa), "r"(sfb), "l"(a1), "l"(b1), "r"(i1)
+            : "memory");
+    return ok;
+}
+
 // Non-blocking test of phase `parity` (never suspends the thread).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
