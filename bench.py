@@ -14,9 +14,9 @@ write-flushed times are reported beside it), the 8192^3 arbitrary-scale GEMM
 with outliers (promotion path; also with the path pinned), the block
 quantization of 8192x8192 bf16 activations (GB/s against HBM), the 4096^3 GEMM
 with per-token x per-channel scales, the 4096^3 GEMM with a fused residual
-add, the per-token-scale 4096^3 GEMMs, and the prefill GEMM with its output
-quantized to E4M3 in the epilogue (beside the same work unfused: the bf16 GEMM
-followed by the block quantizer).  Every generated input buffer is recorded by
+add, the per-token-scale 4096^3 GEMMs (fp32 scales, and UE8M0 bytes), and the
+prefill GEMM with its output quantized to E4M3 in the epilogue (beside the same
+work unfused: the bf16 GEMM followed by the block quantizer).  Every generated input buffer is recorded by
 its SHA-256, with the torch version that generated it.
 
 ``--impl reference`` times the CPU oracle (the only other implementation of
@@ -58,6 +58,8 @@ WORKLOAD_NAMES = {
     "q8": "block quantization of bf16 activations 8192x8192 -> E4M3 codes + 32x32 fp32 scales",
     "r1": "per-token x per-channel scaled E4M3 GEMM M=N=K=4096 (fp32 scales [M] and [N]), bf16 out",
     "f1": "block-scaled E4M3 GEMM M=N=K=4096 with a bf16 residual added in the epilogue",
+    "p1e": ("per-token A scales as UE8M0 bytes (one per row per 32-K block) x 32x32 pow2 B blocks, "
+            "E4M3 GEMM M=N=K=4096 (native path), bf16 out"),
     "qo": ("block-scaled E4M3 GEMM M=8192, N=28672, K=8192 (pow2 32x32 scales) whose output is quantized "
            "in the epilogue to E4M3 codes + 32x32 fp32 scales"),
     "p1": "per-token A scales (one fp32 per row per 32-K block) x 32x32 B blocks, E4M3 GEMM M=N=K=4096, bf16 out",
@@ -249,6 +251,16 @@ def make_runner(name, dev, bs):
         def run(stream):
             bs.fp8_gemm_blockscaled_residual(p.A, p.sA, p.B, p.sB, R, C, p.M, p.N, p.K, stream=stream)
         return run, p.flops, p.algorithmic_bytes + 2 * p.M * p.N, {"A": p.A, "sA": p.sA, "B": p.B, "sB": p.sB, "R": R}
+    if name == "p1e":
+        p = workloads.make("c1", seed=0, device=dev)
+        g = torch.Generator(device=dev).manual_seed(2)
+        e = torch.randint(127 - 4, 127 + 5, (p.M, p.K // 32), generator=g, device=dev).to(torch.uint8)
+        C = torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)
+        nbytes = p.M * p.K + p.N * p.K + e.numel() + 4 * p.sB.numel() + 2 * p.M * p.N
+
+        def run(stream):
+            bs.fp8_gemm_pertoken_e8m0(p.A, e, p.B, p.sB, C, p.M, p.N, p.K, stream=stream)
+        return run, p.flops, nbytes, {"A": p.A, "sA": e, "B": p.B, "sB": p.sB}
     if name in ("p1", "p1n"):
         p = workloads.make("c1", seed=0, device=dev)
         g = torch.Generator(device=dev).manual_seed(2)
@@ -626,7 +638,8 @@ def run_ours(args):
 
     results = {}
     hashes = {}
-    names = [HEADLINE] + ([] if args.headline_only else ["c1", "c3", "c4", "c4p", "q8", "r1", "f1", "p1", "p1n", "qo"])
+    names = [HEADLINE] + ([] if args.headline_only else ["c1", "c3", "c4", "c4p", "q8", "r1", "f1", "p1", "p1n", "p1e",
+                                                         "qo"])
     if args.only:
         names = [args.only]
     launches = 0
@@ -822,7 +835,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-elements", type=int, default=65536)
-    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "c4p", "q8", "r1", "f1", "p1", "p1n", "qo"], default=None,
+    ap.add_argument("--only", choices=["c1", "c2", "c3", "c4", "c4p", "q8", "r1", "f1", "p1", "p1n", "p1e", "qo"],
+                    default=None,
                     help="time one workload only (no e2e, no CPU baseline): profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:

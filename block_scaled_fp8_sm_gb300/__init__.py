@@ -18,7 +18,7 @@ from ._abi import (FP8_PATH_AUTO, FP8_PATH_NATIVE, FP8_PATH_PROMOTE,  # noqa: F4
 __all__ = ["fp8_gemm_blockscaled", "fp8_gemm_blockscaled_noalloc", "fp8_gemm_grouped", "group_descs",
            "fp8_gemm_grouped_device", "fp8_grouped_workspace_bytes", "group_table", "fp8_gemm_pertoken",
            "fp8_quantize_blocks", "fp8_gemm_rowcol", "fp8_gemm_blockscaled_residual",
-           "fp8_gemm_blockscaled_quant", "fp8_status_query", "fp8_strerror", "fp8_version", "fp8_debug_set", "fp8_lib_shutdown",
+           "fp8_gemm_blockscaled_quant", "fp8_gemm_pertoken_e8m0", "fp8_status_query", "fp8_strerror", "fp8_version", "fp8_debug_set", "fp8_lib_shutdown",
            "Fp8Error", "library"]
 
 
@@ -105,6 +105,18 @@ def fp8_gemm_blockscaled_quant(A, sA, B, sB, Cq, sC, M=None, N=None, K=None, str
     _check(library().fp8_gemm_blockscaled_quant(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(Cq), _ptr(sC),
                                                 M, N, K, _stream(stream)), "fp8_gemm_blockscaled_quant")
     return Cq, sC
+
+
+def fp8_gemm_pertoken_e8m0(A, sA, B, sB, C, M=None, N=None, K=None, stream=None):
+    """C = bf16(sum_kb 2^(sA[m][kb]-127) * sB * sum_k A*B): per-token A scales as
+    UE8M0 bytes (uint8 [M, K/32]), B block scales fp32 powers of two; the
+    native path."""
+    M = A.shape[0] if M is None else M
+    K = A.shape[1] if K is None else K
+    N = B.shape[0] if N is None else N
+    _check(library().fp8_gemm_pertoken_e8m0(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C), M, N, K,
+                                            _stream(stream)), "fp8_gemm_pertoken_e8m0")
+    return C
 
 
 def fp8_gemm_rowcol(A, sA, B, sB, C, M=None, N=None, K=None, stream=None):

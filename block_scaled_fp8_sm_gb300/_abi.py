@@ -39,7 +39,7 @@ EXPORTS = (
     "fp8_debug_set", "fp8_lib_shutdown", "fp8_gemm_blockscaled_noalloc",
     "fp8_quantize_blocks", "fp8_gemm_rowcol", "fp8_gemm_blockscaled_residual",
     "fp8_gemm_grouped_device", "fp8_grouped_workspace_bytes", "fp8_gemm_pertoken", "fp8_gemm_pertoken_ex",
-    "fp8_gemm_blockscaled_quant",
+    "fp8_gemm_blockscaled_quant", "fp8_gemm_pertoken_e8m0",
 )
 
 
@@ -80,6 +80,8 @@ def load(path: str = None) -> ctypes.CDLL:
     lib.fp8_gemm_blockscaled_residual.restype = ci
     lib.fp8_gemm_blockscaled_quant.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp]
     lib.fp8_gemm_blockscaled_quant.restype = ci
+    lib.fp8_gemm_pertoken_e8m0.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
+    lib.fp8_gemm_pertoken_e8m0.restype = ci
     lib.fp8_gemm_grouped.argtypes = [ctypes.POINTER(fp8_group_desc), vp, i64, i64, i32, vp]
     lib.fp8_gemm_grouped.restype = ci
     lib.fp8_gemm_grouped_ex.argtypes = [ctypes.POINTER(fp8_group_desc), vp, i64, i64, i32, ci, vp]

@@ -81,6 +81,9 @@ int set_kernel_attrs() {
     if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN, SCALE_TOKEN, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BN, true, false, true>()) != cudaSuccess)
         return FP8_ERR_CUDA;
+    if (cudaFuncSetAttribute(bsfp8_gemm_pair<BN, SCALE_TOKEN_E8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<BN, true, false, true>()) != cudaSuccess)
+        return FP8_ERR_CUDA;
     return FP8_OK;
 }
 
@@ -357,8 +360,8 @@ int launch_pair(const void *A, const float *sA, const void *B, const float *sB, 
         if (rc != FP8_OK) return rc;
     }
     const int pairs = args.c.num_tiles < d->sm_count / 2 ? args.c.num_tiles : d->sm_count / 2;
-    bsfp8_gemm_pair<BN, SK, RES, QOUT>
-        <<<2 * pairs, NUM_THREADS, smem_bytes<BN, true, false, SK == SCALE_TOKEN>(), stream>>>(args);
+    constexpr bool ROWA = SK == SCALE_TOKEN || SK == SCALE_TOKEN_E8;   // per-row A scale lines
+    bsfp8_gemm_pair<BN, SK, RES, QOUT><<<2 * pairs, NUM_THREADS, smem_bytes<BN, true, false, ROWA>(), stream>>>(args);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -675,6 +678,25 @@ int fp8_gemm_pertoken_ex(const void *A, const float *sA, const void *B, const fl
 int fp8_gemm_pertoken(const void *A, const float *sA, const void *B, const float *sB, void *C,
                       int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     return fp8_gemm_pertoken_ex(A, sA, B, sB, C, M, N, K, FP8_PATH_AUTO, stream);
+}
+
+int fp8_gemm_pertoken_e8m0(const void *A, const void *sA, const void *B, const float *sB, void *C,
+                           int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    int rc = check_shape(M, N, K);
+    if (rc != FP8_OK) return rc;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!C) return FP8_ERR_NULL;
+    if (!aligned(C, 16)) return FP8_ERR_ALIGN;
+    if (K > 0) {
+        if (!A || !B || !sA || !sB) return FP8_ERR_NULL;
+        if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sB, 4)) return FP8_ERR_ALIGN;
+    }
+    DeviceState *d = nullptr;
+    rc = device_setup(&d);
+    if (rc != FP8_OK) return rc;
+    if (K == 0) return zero_fill(C, M * N, stream);
+    return launch_pair<TILE_N, SCALE_TOKEN_E8, false>(A, static_cast<const float *>(sA), B, sB, C, M, N, K,
+                                                      FP8_PATH_NATIVE, d, stream);
 }
 
 int fp8_gemm_blockscaled_noalloc(const void *A, const float *sA, const void *B, const float *sB,

@@ -97,10 +97,13 @@ enum : int { PATH_AUTO = 0, PATH_NATIVE = 1, PATH_PROMOTE = 2 };
 // SCALE_BLOCK32: sA [ceil(M/32)][K/32], sB [N/32][K/32] block scales.
 // SCALE_ROWCOL: sA [M] and sB [N], constant along K: the MMAs run with unit
 // scales and the epilogue multiplies each output by sA[m] * sB[n].
-// SCALE_TOKEN: sA [M][K/32], one scale per row of A per 32-K block (per token),
-// sB [N/32][K/32] blocks: always the promotion path, the epilogue thread of
-// row m reading sA[m][kb] itself.
-enum : int { SCALE_BLOCK32 = 0, SCALE_ROWCOL = 1, SCALE_TOKEN = 2 };
+// SCALE_TOKEN: sA [M][K/32] fp32, one scale per row of A per 32-K block (per
+// token), sB [N/32][K/32] blocks: single CTAs take the promotion path (the
+// epilogue thread of row m reads sA[m][kb] itself), CTA pairs the native path
+// with per-row scale lines built by warp 2.
+// SCALE_TOKEN_E8: the same with sA as UE8M0 bytes (2^(e-127)): CTA pairs only,
+// native path; warp 2 copies the bytes into the lines without converting them.
+enum : int { SCALE_BLOCK32 = 0, SCALE_ROWCOL = 1, SCALE_TOKEN = 2, SCALE_TOKEN_E8 = 3 };
 
 template <int BN_, bool PAIR_ = false, bool GROUPED_ = false, bool ROWA_ = false>
 struct Cfg {
@@ -604,7 +607,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     static_assert(!QOUT || (PAIR && !RES && SK == SCALE_BLOCK32), "quantized output: block-scaled pair kernel");
     // per-token scales run the native path on CTA pairs (per-row scale lines)
     // and the promotion path on single CTAs
-    using C = Cfg<BN, PAIR, GROUPED, PAIR && SK == SCALE_TOKEN>;
+    using C = Cfg<BN, PAIR, GROUPED, PAIR && (SK == SCALE_TOKEN || SK == SCALE_TOKEN_E8)>;
+    static_assert(SK != SCALE_TOKEN_E8 || PAIR, "UE8M0 per-token scales: CTA pairs");
     static_assert(!(PAIR && GROUPED), "CTA pairs are used for single problems only");
     constexpr int S = C::STAGES;
     constexpr int NBB = C::NBB;
@@ -1036,7 +1040,105 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
         }
         __syncwarp();
     } else if (warp == 2) {
-        if constexpr (C::ROWA) {
+        if constexpr (C::ROWA && SK == SCALE_TOKEN_E8) {
+            // ------------------------------------ per-row A scale lines, UE8M0 bytes
+            // As below, but sA holds the UE8M0 bytes themselves: lane l loads the
+            // 8 bytes (one per 32-K block of the 256-K entry) of rows l, 32+l, 64+l
+            // and 96+l, and word w of half h's line is bytes 4h..4h+3 of row 32w+l:
+            // no conversion, and a quarter of the fp32 path's load bytes.  A byte
+            // 0xFF (not a number in UE8M0) sets the status word's scale bit.
+            constexpr int H = C::HALVES;
+            static_assert(H == 2, "UE8M0 lines: 256-K entries");
+            const int KW = (c.KS + H - 1) / H;
+            const int total = my_tiles * KW;
+            int il = -1, kl = KW;
+            bool vec = false;   // every row starts on 8 bytes and holds whole entries
+            const uint8_t *lp[4] = {nullptr, nullptr, nullptr, nullptr};
+            auto load = [&](uint2 (&dst)[4]) {
+                if (++kl >= KW) {
+                    kl = 0;
+                    ++il;
+                    const Tile tt = sch.tile(unit + il * nunits);
+                    const uint8_t *sa = reinterpret_cast<const uint8_t *>(sch.entry(tt.g).sA);
+                    vec = (c.KB & 7) == 0 && (reinterpret_cast<uintptr_t>(sa) & 7u) == 0;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int row = tt.m0 + row_off + 32 * w + lane;
+                        lp[w] = row < tt.Mg ? sa + static_cast<int64_t>(row) * c.KB : nullptr;
+                    }
+                }
+                const int kb0 = kl * 8;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    if (vec) {
+                        dst[w] = lp[w] != nullptr ? __ldg(reinterpret_cast<const uint2 *>(lp[w] + kb0))
+                                                  : make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+                    } else {
+                        uint32_t b[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            b[j] = (lp[w] != nullptr && kb0 + j < c.KB) ? __ldg(lp[w] + kb0 + j) : 0x7Fu;
+                        dst[w] = make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                                            b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+                    }
+                }
+            };
+            int ib = -1, kbs = KW, fb = 0;
+            uint32_t phb = 0;
+            auto build = [&](const uint2 (&src)[4]) -> bool {
+                if (++kbs >= KW) {
+                    kbs = 0;
+                    ++ib;
+                    const int v = ib & 1;
+                    if (!__all_sync(FULL, wait_bar(&ctl->vempty[v], (static_cast<uint32_t>(ib >> 1) & 1u) ^ 1u, ctl, c)))
+                        return false;
+                    if (lane == 0) {
+                        ctl->verdict[v] = 0;
+                        mbar_arrive(&ctl->vfull[v]);
+                        trace_event(c, TR_VERDICT, ib);
+                    }
+                    __syncwarp();
+                }
+                const int f = fb;
+                if (!__all_sync(FULL, wait_bar(&ctl->sfempty[f], phb ^ 1u, ctl, c))) return false;
+                if (++fb == FS) {
+                    fb = 0;
+                    phb ^= 1u;
+                }
+                uint8_t *line = sm_sf + f * C::SF_ENTRY + lane * 16;
+                *reinterpret_cast<uint4 *>(line) = make_uint4(src[0].x, src[1].x, src[2].x, src[3].x);
+                *reinterpret_cast<uint4 *>(line + C::SF_BYTES) = make_uint4(src[0].y, src[1].y, src[2].y, src[3].y);
+                // a byte 0xFF: its complement has a zero byte
+                bool bad = false;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t x0 = ~src[w].x, x1 = ~src[w].y;
+                    bad |= (((x0 - 0x01010101u) & ~x0 & 0x80808080u) | ((x1 - 0x01010101u) & ~x1 & 0x80808080u)) != 0u;
+                }
+                if (__any_sync(FULL, bad) && lane == 0) atomicOr(c.status, STATUS_SCALE);
+                fence_proxy_async_smem();   // the lines become visible to tcgen05.cp
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->sfready[f]);
+                __syncwarp();
+                return true;
+            };
+            // four entries in flight (an eight-deep unrolled ring measured 1386
+            // against 1810 TFLOP/s on the 4096^3 GEMM)
+            uint2 r0[4], r1[4], r2[4], r3[4];
+            if (total > 0) load(r0);
+            if (total > 1) load(r1);
+            if (total > 2) load(r2);
+            for (int e = 0; e < total; e += 4) {
+                if (e + 3 < total) load(r3);
+                if (!build(r0) || e + 1 >= total) break;
+                if (e + 4 < total) load(r0);
+                if (!build(r1) || e + 2 >= total) break;
+                if (e + 5 < total) load(r1);
+                if (!build(r2) || e + 3 >= total) break;
+                if (e + 6 < total) load(r2);
+                if (!build(r3)) break;
+            }
+        } else if constexpr (C::ROWA) {
             // ----------------------------------------------- per-row A scale lines
             // Per-token A scales (one per row per 32-K block) on the native path.
             // For each scale-ring entry lane l writes line l of each 128-K half:
@@ -1314,7 +1416,8 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
                     const GroupEntry e = sch.entry(tt.g);
                     const int mb = (tt.m0 + row_off) / 32 + (lane >> 2);
                     const int nb = tt.n0 / 32 + (lane >> 2);
-                    a_in = lane < 16 && mb < (tt.Mg + 31) / 32 && SK != SCALE_TOKEN;   // (per-row sA: read by the epilogue)
+                    // (per-row sA: read by the epilogue or by warp 2)
+                    a_in = lane < 16 && mb < (tt.Mg + 31) / 32 && SK != SCALE_TOKEN && SK != SCALE_TOKEN_E8;
                     b_in = lane < 4 * NBB && nb < c.N / 32;
                     pa = e.sA + (a_in ? static_cast<int64_t>(mb) * c.KB + (lane & 3) : 0);
                     pb = e.sB + (b_in ? static_cast<int64_t>(nb) * c.KB + (lane & 3) : 0);

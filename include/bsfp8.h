@@ -179,6 +179,23 @@ int fp8_gemm_pertoken(const void *A, const float *sA, const void *B, const float
 int fp8_gemm_pertoken_ex(const void *A, const float *sA, const void *B, const float *sB, void *C,
                          int64_t M, int64_t N, int64_t K, int mode, cudaStream_t stream);
 
+/* Per-token A scales given as UE8M0 bytes, the exponent-only 8-bit scale
+ * format of the block-scaled MMA (FP8 GEMM library article,
+ * hncyxsy.com/news/241433, section 2.2, per-token granularity):
+ *   C[m,n] = bf16( sum_kb 2^(sA[m][kb] - 127) * sB[n/32][kb] * sum_k A*B )
+ * sA: uint8 [M, K/32] row-major, any alignment (rows that start on 8 bytes
+ * with K a multiple of 256 are read 8 bytes at a time); a byte 0xFF (not a
+ * number in UE8M0) is reported as FP8_ERR_SCALE through fp8_status_query.
+ * sB: fp32 [N/32, K/32] powers of two (else FP8_ERR_SCALE, as NATIVE mode).
+ * Always the native path (CTA pairs, the bytes copied into per-row scale
+ * lines without conversion); its results equal fp8_gemm_pertoken_ex with
+ * FP8_PATH_NATIVE and the same scales given as fp32 powers of two, bit for
+ * bit.  Scale products below the fp32 normal range (2^-126) may be flushed.
+ * Everything else as fp8_gemm_pertoken.  Returns FP8_OK or FP8_ERR_SHAPE /
+ * FP8_ERR_NULL / FP8_ERR_ALIGN / FP8_ERR_CUDA. */
+int fp8_gemm_pertoken_e8m0(const void *A, const void *sA, const void *B, const float *sB, void *C,
+                           int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* Block quantization of activations to the operand format above (FP8 GEMM
  * library article, hncyxsy.com/news/241433, section 2.1: E4M3, largest value
  * 448; section 2.2: one scale per 32x32 block).  For each 32x32 block of x:

@@ -88,6 +88,20 @@ def test_quant_out_argument_errors(lib):
     assert call(A=0, sA=0, B=0, sB=0, Cq=0, sC=0, M=0) == _abi.FP8_OK
 
 
+def test_pertoken_e8m0_argument_errors(lib):
+    def call(**kw):
+        a = dict(A=16, sA=1, B=16, sB=16, C=16, M=64, N=64, K=64)
+        a.update(kw)
+        return lib.fp8_gemm_pertoken_e8m0(a["A"], a["sA"], a["B"], a["sB"], a["C"], a["M"], a["N"], a["K"], None)
+    assert call(N=33) == _abi.FP8_ERR_SHAPE
+    assert call(K=48) == _abi.FP8_ERR_SHAPE
+    assert call(C=0) == _abi.FP8_ERR_NULL
+    assert call(sA=0) == _abi.FP8_ERR_NULL
+    assert call(C=8) == _abi.FP8_ERR_ALIGN
+    assert call(sB=2) == _abi.FP8_ERR_ALIGN
+    assert call(A=0, sA=0, B=0, sB=0, C=0, M=0) == _abi.FP8_OK
+
+
 def test_empty_problems_enqueue_nothing(lib):
     # M == 0 or N == 0: OK without any device work (no device needed)
     assert _call(lib, A=0, sA=0, B=0, sB=0, C=0, M=0) == _abi.FP8_OK

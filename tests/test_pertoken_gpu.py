@@ -223,3 +223,81 @@ def test_pertoken_native_square_4096_rows(bs):
     Cr, T = oracle.gemm_pertoken(Ah[rows], sAh[rows], Bh, sBh, len(rows), N, K)   # whole rows
     Cg = C[torch.from_numpy(rows).to(DEV)]
     check(bf16_to_f64(Cg), Cr, T, "pertoken native 4096^3 rows")
+
+
+# ------------------------------------------------- UE8M0 per-token scales
+# fp8_gemm_pertoken_e8m0: sA as UE8M0 bytes (value 2^(e-127)); the oracle
+# takes the same scales as fp32 powers of two.
+
+def _e8_problem(M, N, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    A = workloads.normal_codes(M, K, g, "cpu")
+    B = workloads.normal_codes(N, K, g, "cpu")
+    e = torch.randint(127 - 6, 127 + 7, (M, K // 32), generator=g).to(torch.uint8)
+    sA_f32 = torch.ldexp(torch.ones(M, K // 32), e.to(torch.int32) - 127).float()
+    sB = workloads.pow2_scales(N, K // 32, -4, 4, g, "cpu")
+    return A, e.contiguous(), sA_f32.contiguous(), B, sB.contiguous()
+
+
+def _run_e8(bs, A, e, B, sB, M, N, K):
+    buf = torch.full((M + 2, N), -7.0, dtype=torch.bfloat16, device=DEV)
+    C = buf[1:M + 1]
+    bs.fp8_gemm_pertoken_e8m0(A.to(DEV), e.to(DEV) if e.device.type == "cpu" else e, B.to(DEV), sB.to(DEV),
+                              C, M, N, K)
+    torch.cuda.synchronize()
+    assert torch.all(buf[0] == -7.0) and torch.all(buf[-1] == -7.0), "store outside C"
+    return C
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (77, 256, 160), (256, 512, 1024), (300, 288, 2048),
+                                   (1000, 768, 1056)])
+def test_pertoken_e8m0_parity_and_equals_fp32_native(bs, M, N, K):
+    """Against the oracle with the scales as fp32 powers of two, and bit for
+    bit against fp8_gemm_pertoken's native path given those fp32 scales.  K=160
+    and 1056 are not multiples of 256 (bytes read one at a time)."""
+    A, e, sA32, B, sB = _e8_problem(M, N, K, seed=3 * M + N + K)
+    C = _run_e8(bs, A, e, B, sB, M, N, K)
+    assert bs.fp8_status_query() == 0
+    Cr, T = oracle.gemm_pertoken(A.numpy(), sA32.numpy(), B.numpy(), sB.numpy(), M, N, K)
+    check(bf16_to_f64(C), Cr, T, f"pertoken e8m0 {M}x{N}x{K}")
+    C32 = _run_native(bs, A, sA32, B, sB, M, N, K)
+    assert bs.fp8_status_query() == 0
+    assert torch.equal(C.view(torch.int16), C32.view(torch.int16))
+
+
+def test_pertoken_e8m0_unaligned_bytes(bs):
+    """sA starting one byte into an allocation (read byte by byte) gives the
+    same bits as an aligned copy (read 8 bytes at a time)."""
+    M, N, K = 300, 256, 2048
+    A, e, _, B, sB = _e8_problem(M, N, K, seed=21)
+    C_ref = _run_e8(bs, A, e, B, sB, M, N, K)
+    buf = torch.empty(e.numel() + 1, dtype=torch.uint8, device=DEV)
+    e_off = buf[1:].view(e.shape)
+    e_off.copy_(e.to(DEV))
+    assert e_off.data_ptr() % 8 == 1
+    C = _run_e8(bs, A, e_off, B, sB, M, N, K)
+    assert bs.fp8_status_query() == 0
+    assert torch.equal(C.view(torch.int16), C_ref.view(torch.int16))
+
+
+def test_pertoken_e8m0_reports_nan_byte(bs):
+    M, N, K = 300, 512, 1024
+    A, e, _, B, sB = _e8_problem(M, N, K, seed=22)
+    e[211, 17] = 0xFF
+    _run_e8(bs, A, e, B, sB, M, N, K)
+    assert bs.fp8_status_query() == bs._abi.FP8_ERR_SCALE
+    assert bs.fp8_status_query() == 0
+
+
+def test_pertoken_e8m0_square_4096_rows(bs):
+    """4096^3 (several tiles per CTA pair, the byte pipeline crossing tile
+    boundaries, eight entries in flight): whole rows against the oracle."""
+    M = N = K = 4096
+    A, e, sA32, B, sB = _e8_problem(M, N, K, seed=23)
+    C = _run_e8(bs, A, e, B, sB, M, N, K)
+    assert bs.fp8_status_query() == 0
+    rng = np.random.default_rng(23)
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, 2049, M - 1], rng.integers(0, M, 40)]))
+    Cr, T = oracle.gemm_pertoken(A.numpy()[rows], sA32.numpy()[rows], B.numpy(), sB.numpy(), len(rows), N, K)
+    Cg = C[torch.from_numpy(rows).to(DEV)]
+    check(bf16_to_f64(Cg), Cr, T, "pertoken e8m0 4096^3 rows")
