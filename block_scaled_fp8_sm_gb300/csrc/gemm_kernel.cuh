@@ -715,11 +715,10 @@ __device__ __forceinline__ void gemm_body(const Args &args, uint8_t *smem_raw) {
     const uint32_t tmem = ctl->tmem_base;
     const int num_tiles = ctl->num_tiles;
     // Grouped launches use only as many CTAs as give each the same number of
-    // tiles (the tile count is known here, from the device row counts): every
-    // CTA streams its weights at a rate bounded by the bytes it holds in
-    // flight, so a last round with fewer CTAs would run below the memory's
-    // bandwidth (16 groups of 4096 x 7168 weights, 256 tiles: 128 CTAs with
-    // two each take 90 us, 152 CTAs of which 104 take a second tile 93 us).
+    // tiles (the tile count is known here, from the device row counts): a last
+    // round with fewer CTAs than the others measured slower (16 groups of
+    // 4096 x 7168 weights, 256 tiles: 128 CTAs with two each take 90 us, 152
+    // CTAs of which 104 take a second tile 93 us).
     int nunits = grid_units;
     if constexpr (GROUPED) {
         const int rounds = (num_tiles + grid_units - 1) / grid_units;
