@@ -12,8 +12,9 @@
 //                       output tiles, one M=256/N=256/K=32 MMA per 32-K block
 //                       issued by the pair's leader; operand stages of 256 K
 //                       arrive as one 3D TMA box per operand; template
-//                       variants for per-row/column scales and a fused
-//                       residual add
+//                       variants for per-row/column scales, per-token A
+//                       scales (fp32 or UE8M0 bytes), a fused residual add
+//                       and an output quantized to E4M3 with 32x32 scales
 //   bsfp8_gemm_plain    single problems, one CTA per 128 x 256 tile (the
 //                       allocation-free entry point, and the promotion path
 //                       when the caller pins it: with no cross-CTA releases
@@ -23,7 +24,8 @@
 // An M=128 MMA costs ~116 cycles for any N <= 128 but only ~160 for N = 256,
 // so N = 256 is what reaches the tensor peak.  The MMA issue blocks until the
 // pipe accepts the next MMA (it holds about one), so the issuing thread does
-// as little as possible between MMAs.
+// as little as possible between MMAs, and no warp of its sub-partition polls
+// or computes while it issues (two busy neighbours halve its issue rate).
 //
 // Roles (384 threads, one CTA per SM, persistent over output tiles; in a pair
 // each CTA runs every role on its half: both CTAs' operand loads complete on
@@ -32,24 +34,28 @@
 //   warp 0     producer: TMA loads of the A and B K-slices into a ring of
 //              shared-memory stages (128-byte swizzle; grouped problems: A
 //              rows by cp.async).
-//   warp 1     MMA issuer.  Native path: lane 0 copies a stage's UE8M0 scale
-//              lines into tensor memory (tcgen05.cp) and issues its
-//              kind::mxf8f6f4 block-scaled MMAs back to back, testing the next
-//              stage's barriers before the last one.  Promotion path: lane 0
-//              issues one unscaled kind::f8f6f4 MMA and one commit per 32-K
-//              block into one of two tensor-memory partials (a commit holds
-//              the tensor pipe for a few hundred cycles, so partials are as
-//              wide as tensor memory allows); the warp releases a stage's
-//              scale entry once the epilogue has read all of its partials.
+//   warp 1     MMA issuer, run by lane 0 alone.  Native path: it copies a
+//              stage's UE8M0 scale lines into tensor memory (tcgen05.cp) and
+//              issues its kind::mxf8f6f4 block-scaled MMAs back to back as one
+//              straight line, testing the next stage's barriers inside the asm
+//              block of the last two.  Promotion path: one unscaled
+//              kind::f8f6f4 MMA and one commit per 32-K block into one of two
+//              tensor-memory partials (partials as wide as tensor memory
+//              allows); a stage's scale entry is released once the epilogue
+//              has read all of its partials.
 //   warp 2     path verdict: scans each tile's scales ahead of time and decides
 //              native (all positive normal powers of two) or promotion; the
 //              first tile's scan is shared by warps 1, 2 and 4-11 at start.
+//              With per-token native scales it builds the per-row scale lines
+//              instead.
 //   warp 3     scale warp: cp.async of each stage's fp32 scales into a ring
 //              that runs ahead of the operand ring, then the UE8M0 lines (8
 //              identical 16-byte lines per 128 rows, read four times by
 //              tcgen05.cp) that the MMA warp copies into tensor memory.
-//   warps 4-11 epilogue: native tiles drain the accumulator into registers,
-//              release it to the MMA warp at once, then convert to bf16 and
+//   warps 4-11 epilogue: native tiles drain the accumulator into registers
+//              (one warp per column half polls for it; the others wait in the
+//              half's named barrier), release it to the MMA thread at once,
+//              then convert to bf16 (or to E4M3 codes and block scales) and
 //              write 128 x 32 chunks through a shared-memory staging buffer
 //              with TMA stores (grouped tiles: 16-byte stores); promotion
 //              tiles accumulate acc += (sA*sB) * partial per 32-K block in fp32
