@@ -291,7 +291,7 @@ def test_pertoken_e8m0_reports_nan_byte(bs):
 
 def test_pertoken_e8m0_square_4096_rows(bs):
     """4096^3 (several tiles per CTA pair, the byte pipeline crossing tile
-    boundaries, eight entries in flight): whole rows against the oracle."""
+    boundaries, four entries in flight): whole rows against the oracle."""
     M = N = K = 4096
     A, e, sA32, B, sB = _e8_problem(M, N, K, seed=23)
     C = _run_e8(bs, A, e, B, sB, M, N, K)
