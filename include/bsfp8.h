@@ -190,7 +190,8 @@ int fp8_gemm_pertoken_ex(const void *A, const float *sA, const void *B, const fl
  * Always the native path (CTA pairs, the bytes copied into per-row scale
  * lines without conversion); its results equal fp8_gemm_pertoken_ex with
  * FP8_PATH_NATIVE and the same scales given as fp32 powers of two, bit for
- * bit.  Scale products below the fp32 normal range (2^-126) may be flushed.
+ * bit, for bytes 1-254 (the byte 0, 2^-127, has no fp32 normal counterpart).
+ * Scale products below the fp32 normal range (2^-126) may be flushed.
  * Everything else as fp8_gemm_pertoken.  Returns FP8_OK or FP8_ERR_SHAPE /
  * FP8_ERR_NULL / FP8_ERR_ALIGN / FP8_ERR_CUDA. */
 int fp8_gemm_pertoken_e8m0(const void *A, const void *sA, const void *B, const float *sB, void *C,
