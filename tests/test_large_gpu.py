@@ -1,0 +1,89 @@
+"""Outputs past 2^31 elements: the entry points take M, N, K up to 2^31 - 1
+each, so output offsets need 64-bit arithmetic.  C here is 70000 x 32768
+bf16 (2.29e9 elements, 4.6 GB): rows from 65536 on start beyond element
+offset 2^31 and rows from 32768 on beyond byte offset 2^31.  K = 64 keeps the
+work small.  M = 70000 ends inside a 256-row tile.
+
+Checked: guard rows around C, the device status, and sampled elements plus
+whole rows on both sides of each boundary against the oracle; the quantized
+output (E4M3 codes, 2.29e9 bytes) against the GEMM followed by the block
+quantizer, bit for bit over the whole arrays.  Tolerance: tests/_accept.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._accept import bf16_to_f64, check
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+M, N, K = 70000, 32768, 64
+ROWS = (0, 32767, 32768, 65535, 65536, 65537, 69887, 69888, M - 1)
+
+
+@pytest.fixture(scope="module")
+def bs():
+    import block_scaled_fp8_sm_gb300 as mod
+    from block_scaled_fp8_sm_gb300 import build
+    build.build()
+    mod.library()
+    return mod
+
+
+def _problem(seed, pow2):
+    g = torch.Generator().manual_seed(seed)
+    A = workloads.normal_codes(M, K, g, "cpu")
+    B = workloads.normal_codes(N, K, g, "cpu")
+    if pow2:
+        sA = workloads.pow2_scales(M, K // 32, -4, 4, g, "cpu")
+        sB = workloads.pow2_scales(N, K // 32, -4, 4, g, "cpu")
+    else:
+        sA = torch.rand((M + 31) // 32, K // 32, generator=g) * 2 + 0.05
+        sB = torch.rand(N // 32, K // 32, generator=g) * 2 + 0.05
+    return A, sA, B, sB
+
+
+def _sampled(A, sA, B, sB, C, seed):
+    rng = np.random.default_rng(seed)
+    ms = np.concatenate([rng.integers(0, M, 3000), rng.integers(65536, M, 3000)] +
+                        [np.full(N, r) for r in ROWS])
+    ns = np.concatenate([rng.integers(0, N, 6000)] + [np.arange(N) for _ in ROWS])
+    Cr, T = oracle.gemm_sampled(A.numpy(), sA.numpy(), B.numpy(), sB.numpy(), M, N, K, ms, ns)
+    Cg = C[torch.from_numpy(ms).to(DEV), torch.from_numpy(ns).to(DEV)]
+    return Cg, Cr, T
+
+
+@pytest.mark.parametrize("pow2,mode", [(True, None), (False, None), (False, 2)])
+def test_output_past_2_31_elements(bs, pow2, mode):
+    """AUTO on power-of-two scales (native tiles), AUTO on arbitrary scales
+    (promotion tiles on CTA pairs), PROMOTE (the single-CTA kernel)."""
+    A, sA, B, sB = _problem(seed=31 if pow2 else 32, pow2=pow2)
+    buf = torch.full((M + 2, N), -7.0, dtype=torch.bfloat16, device=DEV)
+    C = buf[1:M + 1]
+    bs.fp8_gemm_blockscaled(A.to(DEV), sA.to(DEV), B.to(DEV), sB.to(DEV), C, M, N, K, mode=mode)
+    torch.cuda.synchronize()
+    assert bs.fp8_status_query() == 0
+    assert torch.all(buf[0] == -7.0) and torch.all(buf[-1] == -7.0), "store outside C"
+    Cg, Cr, T = _sampled(A, sA, B, sB, C, seed=5)
+    check(bf16_to_f64(Cg), Cr, T, f"70000x32768x64 {'pow2' if pow2 else 'arb'} mode {mode}")
+    del buf, C
+    torch.cuda.empty_cache()
+
+
+def test_quantized_output_past_2_31_bytes(bs):
+    A, sA, B, sB = (t.to(DEV) for t in _problem(seed=33, pow2=True))
+    Cq = torch.empty(M, N, dtype=torch.uint8, device=DEV)
+    sC = torch.empty((M + 31) // 32, N // 32, dtype=torch.float32, device=DEV)
+    bs.fp8_gemm_blockscaled_quant(A, sA, B, sB, Cq, sC, M, N, K)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    bs.fp8_gemm_blockscaled(A, sA, B, sB, C, M, N, K)
+    q, s = bs.fp8_quantize_blocks(C)
+    torch.cuda.synchronize()
+    assert bs.fp8_status_query() == 0
+    assert torch.equal(Cq, q)
+    assert torch.equal(sC.view(torch.int32), s.view(torch.int32))
+    del Cq, sC, C, q, s
+    torch.cuda.empty_cache()
