@@ -7,7 +7,9 @@ work small.  M = 70000 ends inside a 256-row tile.
 Checked: guard rows around C, the device status, and sampled elements plus
 whole rows on both sides of each boundary against the oracle; the quantized
 output (E4M3 codes, 2.29e9 bytes) against the GEMM followed by the block
-quantizer, bit for bit over the whole arrays.  Tolerance: tests/_accept.py.
+quantizer, bit for bit over the whole arrays; the per-token x per-channel and
+per-token (1 x 32 along K) scale forms on whole rows, whose oracle takes the
+selected rows of A and of their scales.  Tolerance: tests/_accept.py.
 """
 import numpy as np
 import pytest
@@ -86,4 +88,57 @@ def test_quantized_output_past_2_31_bytes(bs):
     assert torch.equal(Cq, q)
     assert torch.equal(sC.view(torch.int32), s.view(torch.int32))
     del Cq, sC, C, q, s
+    torch.cuda.empty_cache()
+
+
+def _guarded():
+    buf = torch.full((M + 2, N), -7.0, dtype=torch.bfloat16, device=DEV)
+    return buf, buf[1:M + 1]
+
+
+def _rows_check(buf, C, Cr, T, what):
+    assert torch.all(buf[0] == -7.0) and torch.all(buf[-1] == -7.0), "store outside C"
+    rows = torch.tensor(ROWS, device=DEV)
+    check(bf16_to_f64(C[rows]), Cr, T, what)
+
+
+def test_rowcol_past_2_31_elements(bs):
+    g = torch.Generator().manual_seed(34)
+    A = workloads.normal_codes(M, K, g, "cpu")
+    B = workloads.normal_codes(N, K, g, "cpu")
+    sA = (torch.rand(M, generator=g) * 4 - 2).float()
+    sB = (torch.rand(N, generator=g) * 3).float()
+    buf, C = _guarded()
+    bs.fp8_gemm_rowcol(A.to(DEV), sA.to(DEV), B.to(DEV), sB.to(DEV), C, M, N, K)
+    torch.cuda.synchronize()
+    assert bs.fp8_status_query() == 0
+    r = list(ROWS)
+    Cr, T = oracle.gemm_rowcol(A.numpy()[r], sA.numpy()[r], B.numpy(), sB.numpy(), len(r), N, K)
+    _rows_check(buf, C, Cr, T, "rowcol 70000x32768x64 rows")
+    del buf, C
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("form", ["promote", "e8m0"])
+def test_pertoken_past_2_31_elements(bs, form):
+    """Arbitrary per-token scales (AUTO: the single-CTA promotion kernel) and
+    UE8M0 bytes (the native CTA-pair kernel)."""
+    g = torch.Generator().manual_seed(35)
+    A = workloads.normal_codes(M, K, g, "cpu")
+    B = workloads.normal_codes(N, K, g, "cpu")
+    sB = workloads.pow2_scales(N, K // 32, -4, 4, g, "cpu")
+    buf, C = _guarded()
+    if form == "promote":
+        sA = (torch.rand(M, K // 32, generator=g) * 2 + 0.05).float()
+        bs.fp8_gemm_pertoken(A.to(DEV), sA.to(DEV), B.to(DEV), sB.to(DEV), C, M, N, K)
+    else:
+        e = torch.randint(127 - 6, 127 + 7, (M, K // 32), generator=g).to(torch.uint8)
+        sA = torch.ldexp(torch.ones(M, K // 32), e.to(torch.int32) - 127).float()
+        bs.fp8_gemm_pertoken_e8m0(A.to(DEV), e.to(DEV), B.to(DEV), sB.to(DEV), C, M, N, K)
+    torch.cuda.synchronize()
+    assert bs.fp8_status_query() == 0
+    r = list(ROWS)
+    Cr, T = oracle.gemm_pertoken(A.numpy()[r], sA.numpy()[r], B.numpy(), sB.numpy(), len(r), N, K)
+    _rows_check(buf, C, Cr, T, f"pertoken {form} 70000x32768x64 rows")
+    del buf, C
     torch.cuda.empty_cache()
