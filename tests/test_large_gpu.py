@@ -9,7 +9,8 @@ whole rows on both sides of each boundary against the oracle; the quantized
 output (E4M3 codes, 2.29e9 bytes) against the GEMM followed by the block
 quantizer, bit for bit over the whole arrays; the per-token x per-channel and
 per-token (1 x 32 along K) scale forms on whole rows, whose oracle takes the
-selected rows of A and of their scales.  Tolerance: tests/_accept.py.
+selected rows of A and of their scales; a grouped call whose first group has
+70000 rows.  Tolerance: tests/_accept.py.
 """
 import numpy as np
 import pytest
@@ -141,4 +142,39 @@ def test_pertoken_past_2_31_elements(bs, form):
     Cr, T = oracle.gemm_pertoken(A.numpy()[r], sA.numpy()[r], B.numpy(), sB.numpy(), len(r), N, K)
     _rows_check(buf, C, Cr, T, f"pertoken {form} 70000x32768x64 rows")
     del buf, C
+    torch.cuda.empty_cache()
+
+
+def test_grouped_past_2_31_elements(bs):
+    """The grouped call (64-row tiles, 16-byte global stores) with one group
+    of 70000 rows and one of 5."""
+    Ms = [M, 5]
+    g = torch.Generator().manual_seed(36)
+    probs = []
+    for Mg in Ms:
+        A = workloads.normal_codes(Mg, K, g, "cpu")
+        B = workloads.normal_codes(N, K, g, "cpu")
+        sA = workloads.pow2_scales(Mg, K // 32, -4, 4, g, "cpu")
+        sB = workloads.pow2_scales(N, K // 32, -4, 4, g, "cpu")
+        probs.append((A, sA, B, sB))
+    outs, groups = [], []
+    for Mg, (A, sA, B, sB) in zip(Ms, probs):
+        Cg = torch.full((Mg + 1, N), -7.0, dtype=torch.bfloat16, device=DEV)
+        outs.append(Cg)
+        groups.append((A.to(DEV), sA.to(DEV), B.to(DEV), sB.to(DEV), Cg))
+    bs.fp8_gemm_grouped(groups, torch.tensor(Ms, dtype=torch.int32, device=DEV), N, K)
+    torch.cuda.synchronize()
+    assert bs.fp8_status_query() == 0
+    for Mg, Cg in zip(Ms, outs):
+        assert torch.all(Cg[Mg] == -7.0), "store past M_g"
+    A, sA, B, sB = probs[0]
+    r = [x for x in ROWS]
+    ms = np.concatenate([np.full(N, x) for x in r])
+    ns = np.concatenate([np.arange(N) for _ in r])
+    Cr, T = oracle.gemm_sampled(A.numpy(), sA.numpy(), B.numpy(), sB.numpy(), M, N, K, ms, ns)
+    check(bf16_to_f64(outs[0][torch.tensor(r, device=DEV)].reshape(-1)), Cr, T, "grouped 70000x32768x64 rows")
+    A, sA, B, sB = probs[1]
+    Cr, T = oracle.gemm(A.numpy(), sA.numpy(), B.numpy(), sB.numpy(), 5, N, K)
+    check(bf16_to_f64(outs[1][:5]), Cr, T, "grouped 5x32768x64")
+    del outs, groups
     torch.cuda.empty_cache()
